@@ -1,0 +1,466 @@
+"""Benchmark: verified draft positions/s and achieved HBM GB/s of the verification hot path.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sv|reference] [--workload c1..c5]
+
+One step = one verification round (plus the D-cut schedule for c4) over one batch of synthetic
+logits already resident in HBM, through the library's C ABI.  Rotating input sets whose total
+exceeds the 129 MB L2 keep every step's logits cold in L2.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload (the only other place this file runs oracle code, besides the cpu_baseline leg).
+Under torchrun each rank is an independent replica on its own GPU (weak scaling): requests
+are independent, so there is no data-path collective; only the timing max-reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "c1": "greedy T=0 verify, B=4 K=3 V=32000 bf16, draft tokens fused from draft argmax",
+    "c2": "stochastic MTP-style verify T=1.0, B=16 K=3 V=151936 bf16",
+    "c3": "block-parallel DFly-style verify T=0.6, B=64 K=16 V=151936 fp32",
+    "c4": "D-cut schedule (B=64 D=16 budget 384, c=1+0.05K) + ragged verify T=1.0 V=151936 bf16",
+    "c5": "mixed round c64: 32 chat K=3 + 32 code K=16, T in {0,0.6,1}, V=151936 bf16",
+}
+
+
+def make_sets(workload: str, n_sets: int, base_seed: int):
+    """Synthetic input sets (host numpy) of one workload."""
+    sets = []
+    for j in range(n_sets):
+        seed = base_seed + j
+        if workload == "c1":
+            sets.append({"batch": W.c1_greedy(seed)})
+        elif workload == "c2":
+            sets.append({"batch": W.c2_mtp(seed)})
+        elif workload == "c3":
+            sets.append({"batch": W.c3_dfly(seed)})
+        elif workload == "c4":
+            s = W.c4_alpha(seed)
+            b = W.c4_verify(s, np.full(64, 16, np.int32), seed=seed)
+            sets.append({"batch": b, "sched": s})
+        elif workload == "c5":
+            sets.append({"batch": W.c5_mixed(seed=base_seed, rnd=j)})
+    return sets
+
+
+def algorithmic_bytes(b, keep_len) -> int:
+    """Each needed logit byte once: n_i + 1 target rows, plus n_i draft rows when the request
+    samples (T > 0) or takes its drafted tokens from the draft argmax."""
+    elt = 2 if b.dtype == "bf16" else 4
+    rows = 0
+    for i in range(b.B):
+        n = int(keep_len[i])
+        rows += n + 1
+        if b.temperature[i] > 0 or b.tokens is None:
+            rows += n
+    return rows * b.V * elt
+
+
+# -------------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_74_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per row_stats launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = f"/tmp/sv_clocks_{os.getpid()}.csv"
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    smax.append(float(parts[2].split()[0]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------------------------- GPU arm
+
+class GpuWorkload:
+    def __init__(self, workload, sets, device):
+        import torch
+        import speculative_decoding_verification_74_gb300 as sv
+        self.sv, self.torch, self.dev = sv, torch, device
+        self.workload = workload
+        self.sets = []
+        b0 = sets[0]["batch"]
+        self.dt = sv.SV_BF16 if b0.dtype == "bf16" else sv.SV_F32
+        self.B, self.Kmax, self.V = b0.B, b0.Kmax, b0.V
+        self.ws = sv.workspace(sv.SV_OP_VERIFY, self.B, self.Kmax, self.V, self.dt, device)
+        self.ws_sched = sv.workspace(sv.SV_OP_SCHEDULE, self.B, self.Kmax, 1, sv.SV_F32, device)
+        for s in sets:
+            self.sets.append(self._upload(s))
+        self.out = (torch.empty((self.B, self.Kmax + 1), dtype=torch.int32, device=device),
+                    torch.empty(self.B, dtype=torch.int32, device=device),
+                    torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
+                    torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
+                    torch.empty(self.B, dtype=torch.uint8, device=device))
+        self.sched_out = (torch.empty(self.B, dtype=torch.int32, device=device),
+                          torch.empty(self.B + 1, dtype=torch.int32, device=device),
+                          torch.empty(1, dtype=torch.int32, device=device),
+                          torch.empty(1, dtype=torch.int64, device=device))
+
+    def _t(self, a, dtype=None):
+        torch = self.torch
+        if a is None:
+            return None
+        if dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(self.dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def _upload(self, s):
+        b = s["batch"]
+        d = {"b": b,
+             "target": self._t(b.target, b.dtype), "draft": self._t(b.draft, b.dtype),
+             "t_off": self._t(b.t_offsets), "d_off": self._t(b.d_offsets),
+             "tokens": self._t(b.tokens), "keep": self._t(b.keep_len), "temp": self._t(b.temperature),
+             "rid": self._t(b.request_ids)}
+        if "sched" in s:
+            d["alpha"] = self._t(s["sched"].alpha)
+            d["sched"] = s["sched"]
+        return d
+
+    def step(self, j, stream=None):
+        sv = self.sv
+        d = self.sets[j % len(self.sets)]
+        b = d["b"]
+        if self.workload == "c1":
+            sv.sv_verify_greedy(d["target"], b.V, d["draft"], b.V, None, self.dt, self.B, self.Kmax, self.V,
+                                self.out[0], self.out[1], self.ws, stream)
+        elif self.workload in ("c2", "c3"):
+            sv.sv_verify_sample(d["target"], b.V, d["draft"], b.V, d["tokens"], d["temp"], b.seed, b.round,
+                                d["rid"], self.dt, self.B, self.Kmax, self.V, *self.out, self.ws, stream)
+        else:
+            keep = d["keep"]
+            if self.workload == "c4":
+                s = d["sched"]
+                sv.sv_schedule_depth(d["alpha"], self.Kmax, None, self.B, self.Kmax, s.cost_a, s.cost_b, s.budget,
+                                     None, sv.SV_OBJ_THROUGHPUT, *self.sched_out, self.ws_sched, stream)
+                keep = self.sched_out[0]
+            sv.sv_verify_ragged(d["target"], b.V, d["t_off"], d["draft"], b.V, d["d_off"], d["tokens"], self.Kmax,
+                                keep, d["temp"], b.seed, b.round, d["rid"], self.dt, self.B, self.Kmax, self.V,
+                                *self.out, self.ws, stream)
+
+    def keep_len(self, j):
+        """Kept positions of set j (runs the schedule once for c4)."""
+        d = self.sets[j % len(self.sets)]
+        if self.workload != "c4":
+            return d["b"].keep_len
+        self.step(j)
+        self.torch.cuda.synchronize()
+        return self.sched_out[0].cpu().numpy()
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import speculative_decoding_verification_74_gb300 as sv
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # rotating input sets: enough distinct sets that the working set exceeds L2
+    probe = make_sets(args.workload, 1, 1000 + 7919 * rank)
+    b0 = probe[0]["batch"]
+    set_bytes = algorithmic_bytes(b0, b0.keep_len if args.workload != "c4" else np.full(b0.B, 16))
+    n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))))
+    n_sets = min(n_sets, 200)
+    sets = probe + make_sets(args.workload, n_sets - 1, 1001 + 7919 * rank)
+    gw = GpuWorkload(args.workload, sets, dev)
+
+    keeps = [gw.keep_len(j) for j in range(len(gw.sets))]
+    pos = [int(np.sum(k)) for k in keeps]
+    byts = [algorithmic_bytes(gw.sets[j]["b"], keeps[j]) for j in range(len(gw.sets))]
+    steps, warm = args.steps, args.warmup
+    tot_pos = sum(pos[j % len(pos)] for j in range(warm, warm + steps))
+    tot_bytes = sum(byts[j % len(byts)] for j in range(warm, warm + steps))
+
+    stream = torch.cuda.current_stream()
+    for j in range(warm):
+        gw.step(j)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    launches0 = sv.sv_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for j in range(warm, warm + steps):
+        gw.step(j)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    launches = sv.sv_launch_count() - launches0
+    clk = clocks.stop() if clocks else None
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+
+    # per-kernel durations: an instrumented repeat of the same K steps (CUDA events on the
+    # launching stream around every library kernel)
+    sv.sv_profile_enable(True)
+    for j in range(warm, warm + steps):
+        gw.step(j)
+    kms, kn = sv.sv_profile_collect()
+    sv.sv_profile_enable(False)
+
+    # end to end through host buffers: H2D of the step's inputs from pinned memory, the C ABI
+    # call, D2H of the emitted tokens and accepted lengths
+    e2e = run_e2e(gw, warm, steps, stream)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    k1_avg_ms = kms[sv.SV_KERNEL_ROW_STATS] / max(1, kn[sv.SV_KERNEL_ROW_STATS])
+    k1_bytes = tot_bytes / steps
+    achieved = k1_bytes / (k1_avg_ms * 1e-3) / 1e9
+    cpu = cpu_baseline(args.workload) if world == 1 else None
+    value = world * tot_pos / (ms * 1e-3)
+    line = {
+        "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
+        "value": value, "unit": "positions/s", "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if gw.dt == sv.SV_BF16 else "f32", "data": "synthetic (seeded numpy, recipes in DESIGN.md)",
+        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload]}", "B": gw.B, "Kmax": gw.Kmax, "V": gw.V,
+                   "positions_per_step": tot_pos / steps, "logit_bytes_per_step": k1_bytes,
+                   "l2": f"{len(gw.sets)} rotating input sets, {sum(byts) / 1e6:.0f} MB of logits read > 129 MB L2",
+                   "parallelism": f"replicas x{world} (independent requests, no collective)"},
+        "achieved_gbs_step": tot_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "row_stats", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                     "avg_launch_us": k1_avg_ms * 1e3, "bytes_per_launch": k1_bytes,
+                     "timing": "CUDA events around each row_stats launch, instrumented repeat of the K steps"},
+        "kernels_us_per_step": {sv.KERNEL_NAMES[i]: kms[i] * 1e3 / steps for i in range(sv.SV_NUM_KERNELS)
+                                if kn[i]},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(gw, warm, steps, stream):
+    import torch
+    sv = gw.sv
+    pinned = []
+    names = ("target", "draft", "t_off", "d_off", "tokens", "keep", "temp", "rid", "alpha")
+    for d in gw.sets[:2]:
+        pinned.append({k: d[k].cpu().pin_memory() for k in names if d.get(k) is not None})
+    h_out = [torch.empty(tuple(gw.out[0].shape), dtype=torch.int32).pin_memory(),
+             torch.empty(tuple(gw.out[1].shape), dtype=torch.int32).pin_memory()]
+    # device staging buffers for one set (the step's inputs land here every step)
+    stage = {k: torch.empty_like(gw.sets[0][k]) for k in pinned[0]}
+    h2d = sum(v.numel() * v.element_size() for v in pinned[0].values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out)
+    n = max(1, min(steps, 20))
+    orig = gw.sets
+
+    def one(j):
+        src = pinned[j % 2]
+        for k, v in src.items():
+            stage[k].copy_(v, non_blocking=True)
+        d = dict(orig[j % 2])
+        d.update(stage)
+        gw.sets = [d]
+        gw.step(0)
+        h_out[0].copy_(gw.out[0], non_blocking=True)
+        h_out[1].copy_(gw.out[1], non_blocking=True)
+
+    for j in range(2):
+        one(j)
+    torch.cuda.synchronize()
+    pos = [int(np.sum(gw.keep_len(j))) for j in range(2)] if gw.workload != "c4" else None
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for j in range(n):
+        one(j)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    gw.sets = orig
+    if pos is None:
+        pos = [int(np.sum(gw.keep_len(j))) for j in range(2)]
+    tot = sum(pos[j % 2] for j in range(n))
+    ms = ev0.elapsed_time(ev1)
+    return {"value": tot / (ms * 1e-3), "unit": "positions/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "wall_s": wall,
+            "note": "pinned host inputs copied to the device each step, C ABI call, tokens+lengths copied back"}
+
+
+# -------------------------------------------------------------------------------- CPU oracle
+
+def oracle_step(workload, sets, j, req_slice):
+    from oracle.verify import verify_batch
+    from oracle.schedule import dcut_schedule
+    s = sets[j % len(sets)]
+    b = s["batch"]
+    keep = b.keep_len
+    if workload == "c4":
+        sc = s["sched"]
+        keep = dcut_schedule(sc.alpha, None, sc.cost_a, sc.cost_b, sc.budget)["keep_len"]
+    lo, hi = req_slice
+    sub = slice(lo, hi)
+    verify_batch(b.target, b.t_offsets[lo:], b.draft, b.d_offsets[lo:] if b.d_offsets is not None else None,
+                 None if b.tokens is None else b.tokens[sub], keep[sub], b.temperature[sub], b.seed, b.round,
+                 b.request_ids[sub], b.dtype, b.Kmax)
+    return int(np.sum(keep[sub]))
+
+
+def cpu_baseline(workload, budget_s: float = 15.0):
+    """The oracle, as it stands, on a bounded sample of the workload (single process)."""
+    sets = make_sets(workload, 1, 1000)
+    b = sets[0]["batch"]
+    t0 = time.perf_counter()
+    pos = 0
+    nreq = 0
+    i = 0
+    while time.perf_counter() - t0 < budget_s and nreq < 64 * b.B:
+        pos += oracle_step(workload, sets, 0, (i % b.B, i % b.B + 1))
+        nreq += 1
+        i += 1
+    dt = time.perf_counter() - t0
+    return {"value": pos / dt, "unit": "positions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nreq} requests of the {workload} batch verified one by one by the fp64 numpy oracle "
+                      f"({dt:.1f} s, 1 thread)"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    sets = make_sets(args.workload, 1, 1000)
+    b = sets[0]["batch"]
+    per_step = max(1, min(b.B, 4))
+    for j in range(args.warmup):
+        oracle_step(args.workload, sets, 0, ((j * per_step) % b.B, (j * per_step) % b.B + 1))
+    t0 = time.perf_counter()
+    pos = 0
+    for j in range(args.steps):
+        lo = (j * per_step) % b.B
+        pos += oracle_step(args.workload, sets, 0, (lo, min(b.B, lo + per_step)))
+    dt = time.perf_counter() - t0
+    v = pos / dt
+    line = {"impl": "reference", "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
+            "value": v, "unit": "positions/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy)",
+            "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload]}",
+                       "sample": f"{per_step} requests per step"},
+            "cpu_baseline": {"value": v, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} of {b.B} requests per step, fp64 numpy oracle, 1 thread"},
+            "e2e": {"value": v, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="sv", choices=["sv", "reference"])
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * sv.h -- C ABI of libsv: speculative-decoding draft verification and D-cut
+ * verification-depth scheduling on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages describing AngelSpec, Liu et al., Tencent):
+ *   [explainer]  "AngelSpec: specialize the drafter, share the verification
+ *                budget" (ai.thesatyajit.com/articles/angelspec)
+ *   [release]    tradepoint.io article on the open-source AngelSpec release
+ *   [abstract]   abstract of "AngelSpec: Towards Real-World High Performance
+ *                Inference with Speculative Decoding"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory    All array arguments are DEVICE pointers owned by the caller,
+ *           except `ratios` of sv_schedule_depth (host).  The library never
+ *           allocates device memory.  Scratch comes from a caller workspace
+ *           of at least sv_workspace_size(...) bytes, 256-byte aligned, that
+ *           must be zero-filled once before its first use; the library leaves
+ *           it reusable (its counters return to zero at the end of every
+ *           call).  One workspace must not be used by two calls that may run
+ *           at the same time (different streams).
+ * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *           default stream).  All work is enqueued asynchronously; no call
+ *           synchronizes, except sv_query_status and sv_profile_collect.
+ * Errors    Every call returns an sv_status.  Host-side checks (NULL
+ *           pointers, sizes, alignment, workspace size) return before any
+ *           work is enqueued.  Values that only the device sees (token ids,
+ *           temperatures, kept lengths, row offsets, confidences) are checked
+ *           by the kernels: a bad request gets accept_len = -1 and all tokens
+ *           -1, a bad schedule gets total_K = -1, and a bit is OR-ed into the
+ *           workspace status word, read (and cleared) by sv_query_status.
+ *           The kernels never trap; every wait in them is bounded.
+ * Logits    Rows of V logits, contiguous, bf16 (SV_BF16) or float32
+ *           (SV_F32), finite or -inf (a masked token).  NaN and +inf are not
+ *           valid logits (results unspecified).  Row starts must be 16-byte
+ *           aligned: the base pointer 16-byte aligned and the row stride (in
+ *           elements) times the element size a multiple of 16.
+ * Randomness  The accept test and the resampling draw use Philox4x32-10
+ *           (Salmon et al., SC'11) with key = (seed low, seed high word) and
+ *           counter = (position, request id, purpose, round); purpose 0 is the
+ *           accept test at drafted position k, purpose 1 the draw at position
+ *           a.  u = (word0 >> 8) * 2^-24.
+ */
+#ifndef SV_H_
+#define SV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, stride or alignment   */
+  SV_ERR_WORKSPACE = 2,    /* workspace NULL, misaligned or too small        */
+  SV_ERR_CUDA = 3,         /* a CUDA runtime call failed; see sv_last_error_string */
+  SV_ERR_DEVICE_INPUT = 4, /* sv_query_status: a kernel flagged bad input    */
+  SV_ERR_TIMEOUT = 5       /* sv_query_status: a bounded wait ran out        */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
+
+/* operation ids for sv_workspace_size */
+enum { SV_OP_VERIFY = 0, SV_OP_SCHEDULE = 1 };
+
+/* objective of sv_schedule_depth */
+enum {
+  SV_OBJ_THROUGHPUT = 0, /* maximise U(K) / c(K): projected throughput ([explainer] "D-cut") */
+  SV_OBJ_NET = 1         /* maximise U(K) - c(K): expected utility minus cost ([abstract])    */
+};
+
+/* bits of the device status word */
+enum {
+  SV_DEV_BAD_TOKEN = 1u << 0,       /* drafted token outside [0, V)                  */
+  SV_DEV_BAD_TEMPERATURE = 1u << 1, /* temperature < 0 or NaN                        */
+  SV_DEV_BAD_KEEP_LEN = 1u << 2,    /* keep_len outside [0, Kmax]                    */
+  SV_DEV_BAD_OFFSETS = 1u << 3,     /* row offsets leave fewer rows than needed      */
+  SV_DEV_NO_DRAFT_ROWS = 1u << 4,   /* T > 0 (or greedy without tokens) but draft NULL */
+  SV_DEV_BAD_ALPHA = 1u << 5,       /* confidence outside [0, 1] or NaN              */
+  SV_DEV_BAD_DRAFT_LEN = 1u << 6,   /* draft_len outside [0, Dmax]                   */
+  SV_DEV_TIMEOUT = 1u << 7          /* a bounded wait inside a kernel ran out        */
+};
+
+/* per-request bits of out_flags */
+enum {
+  SV_FLAG_Q_ZERO = 1u << 0, /* q(x) == 0 at some accept test: accepted iff p(x) > 0 */
+  SV_FLAG_Z_ZERO = 1u << 1, /* residual mass 0 at the rejection: drew from p_a       */
+  SV_FLAG_INVALID = 1u << 2 /* the request's input was invalid (outputs are -1)      */
+};
+
+/* Limits (checked on the host). */
+#define SV_MAX_BATCH 4096
+#define SV_MAX_DRAFT 1023
+#define SV_MAX_SCHEDULE_SLOTS 16384 /* sum_i draft_len_i for sv_schedule_depth */
+
+/* ABI version; bumped on any signature change. */
+int sv_abi_version(void);
+
+/* Bytes of workspace that `op` needs for the given sizes (Kmax = largest number
+ * of drafted positions per request; V = vocabulary size; dt = logit dtype).
+ * Returns 0 for invalid sizes. */
+size_t sv_workspace_size(int op, int B, int Kmax, int V, sv_dtype dt);
+
+/*
+ * sv_verify_greedy -- T = 0 verification ([release] "The MTP path": greedy
+ * acceptance; [explainer] "MTP: fix position 2 and 3": one rejection voids
+ * every later position).
+ *
+ * For each request i (0 <= i < B) with K drafted positions:
+ *   g_k = first argmax of target row k (k = 0..K; row K is the bonus row)
+ *   x_k = draft_tokens[i*K + k], or, when draft_tokens is NULL, the first
+ *         argmax of draft row k
+ *   a   = first k with x_k != g_k, else K
+ *   out_tokens[i*(K+1) + j] = x_j for j < a, g_a at j = a, -1 after
+ *   out_accept_len[i] = a
+ * Layout: target row k of request i starts at target + (i*(K+1) + k) *
+ * t_row_stride elements; draft row k at draft + (i*K + k) * d_row_stride.
+ * draft may be NULL when draft_tokens is given (the draft rows are not read).
+ * Exactly one of draft / draft_tokens may be NULL.  B >= 0, 0 <= K <= SV_MAX_DRAFT,
+ * V >= 1.  B == 0 is a no-op.
+ */
+sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void* draft,
+                           int64_t d_row_stride, const int32_t* draft_tokens, sv_dtype dt, int B,
+                           int K, int V, int32_t* out_tokens, int32_t* out_accept_len, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * sv_verify_sample -- lossless rejection-sampling verification in one pass
+ * over the logits ([release] "Why one universal drafter underperforms":
+ * drafted tokens are verified together in one target pass by rejection
+ * sampling; [explainer] "D-cut": verification stays exact).
+ *
+ * Per request i with temperature T = temperature[i] (device, float32):
+ *   T == 0: exactly sv_verify_greedy with the given tokens (draft rows unread);
+ *           out_p = 1 if x_k is the target argmax else 0, out_q = 1.
+ *   T  > 0: p_k = softmax(target_k / T), q_k = softmax(draft_k / T)
+ *           accept k  <=>  u_k * q_k(x_k) < p_k(x_k),  u_k = Philox(purpose 0, k)
+ *           a = first rejected position, else K
+ *           y ~ norm(max(0, p_a - q_a)) when a < K, else y ~ p_K (bonus row),
+ *           drawn by inverse CDF in vocabulary order with u' = Philox(purpose 1, a)
+ *           out_tokens: x_0..x_{a-1}, y, then -1; out_accept_len[i] = a
+ *           out_p / out_q [B*K] (nullable): p_k(x_k), q_k(x_k) for every k < K
+ *           out_flags [B] (nullable): SV_FLAG_* bits
+ * request_ids (nullable => i) names the request in the Philox counter; `round`
+ * is the counter's last word.  Layouts as in sv_verify_greedy; draft_tokens
+ * is required; draft may be NULL only if every temperature is 0.
+ */
+sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void* draft,
+                           int64_t d_row_stride, const int32_t* draft_tokens,
+                           const float* temperature, uint64_t seed, uint32_t round,
+                           const int32_t* request_ids, sv_dtype dt, int B, int K, int V,
+                           int32_t* out_tokens, int32_t* out_accept_len, float* out_p,
+                           float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/*
+ * sv_verify_ragged -- verification of per-request kept prefixes
+ * ([explainer] "D-cut", Figure 3 panel 4: the target verifies only the
+ * surviving tokens of each request).
+ *
+ * As sv_verify_sample, with n_i = keep_len[i] (device, 0 <= n_i <= Kmax)
+ * positions per request and packed rows:
+ *   target row k (0 <= k <= n_i) of request i: target + (t_row_offsets[i] + k) * t_row_stride
+ *   draft  row k (0 <= k <  n_i) of request i: draft  + (d_row_offsets[i] + k) * d_row_stride
+ *   drafted token k: draft_tokens[i * tok_stride + k]
+ * t_row_offsets / d_row_offsets are device int32 [B+1]; the kernels check
+ * t_row_offsets[i+1] - t_row_offsets[i] >= n_i + 1 and the same with n_i for
+ * the draft rows of sampled requests.  d_row_offsets may be NULL when draft is
+ * NULL.  Outputs are [B, Kmax+1] tokens and [B, Kmax] p/q (entries k >= n_i are
+ * NaN).  draft_tokens may be NULL only if every temperature is 0 and draft is
+ * given (x_k = first argmax of draft row k).
+ */
+sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets,
+                           const void* draft, int64_t d_row_stride, const int32_t* d_row_offsets,
+                           const int32_t* draft_tokens, int tok_stride, const int32_t* keep_len,
+                           const float* temperature, uint64_t seed, uint32_t round,
+                           const int32_t* request_ids, sv_dtype dt, int B, int Kmax, int V,
+                           int32_t* out_tokens, int32_t* out_accept_len, float* out_p,
+                           float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/*
+ * sv_schedule_depth -- D-cut batch-shared verification-depth allocation
+ * ([explainer] "D-cut: verification depth is a shared resource", Figure 3
+ * panels 2-3 and eq. K_rho; [abstract]: expected utility with a profiled
+ * cost model).
+ *
+ * alpha [B, alpha_stride] float32 (device): alpha[i*alpha_stride + k-1] is the
+ * drafter's confidence in drafted position k (1 <= k <= D_i), in [0, 1].
+ * draft_len [B] (device, nullable => Dmax) gives D_i.
+ *   s_{i,0} = 1, s_{i,k} = s_{i,k-1} * alpha_{i,k}  (float32, left to right)
+ *   slot 0 of every request is always kept; the other N - B slots
+ *   (N = sum_i (D_i + 1)) are ranked by (s desc, request asc, position asc)
+ *   candidates K = clip(max(B, ceil(rho * N)), B, cap) for rho in ratios
+ *   (host array, NULL => {0.25, 0.5, 0.75, 1.0}, n_ratios <= 8), cap =
+ *   min(budget, N) (budget <= 0 => N); duplicates collapse
+ *   U(K) = sum of round(s * 2^48) over the top K slots (exact int64)
+ *   cost c(K) = cost_a + cost_b * K (float64); objective SV_OBJ_THROUGHPUT
+ *   (U / 2^48 / c) or SV_OBJ_NET (U / 2^48 - c); ties pick the smaller K
+ * Outputs (device): out_keep_len [B] = n_i (kept drafted positions),
+ * out_row_offsets [B+1] (nullable) = packed target-row offsets with n_i + 1
+ * rows per request, out_total_K [1], out_utility_q48 [1] (nullable) = U(K).
+ * Limits: 1 <= B <= SV_MAX_BATCH, 0 <= Dmax <= SV_MAX_DRAFT,
+ * B * Dmax <= SV_MAX_SCHEDULE_SLOTS, budget <= 0 or budget >= B,
+ * cost_a >= 0, cost_b >= 0, cost_a + cost_b > 0.
+ */
+sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t* draft_len, int B,
+                            int Dmax, float cost_a, float cost_b, int budget, const float* ratios,
+                            int n_ratios, int objective, int32_t* out_keep_len,
+                            int32_t* out_row_offsets, int32_t* out_total_K,
+                            int64_t* out_utility_q48, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, returns the workspace's device status word in
+ * *device_status (SV_DEV_* bits) and clears it.  Returns SV_OK if the word was
+ * zero, SV_ERR_TIMEOUT if SV_DEV_TIMEOUT is set, else SV_ERR_DEVICE_INPUT. */
+sv_status sv_query_status(void* ws, void* stream, uint32_t* device_status);
+
+const char* sv_status_string(sv_status s);
+
+/* Text of the last SV_ERR_CUDA / SV_ERR_INVALID_ARG on this host thread. */
+const char* sv_last_error_string(void);
+
+/* Instrumentation.  While enabled, every library kernel launch is bracketed by
+ * CUDA events on its stream.  sv_profile_collect synchronizes the device, adds
+ * the elapsed times per kernel id into total_ms[id] and the launch counts into
+ * launches[id] (arrays of SV_NUM_KERNELS), and forgets the recorded events.
+ * sv_launch_count returns the number of library kernel launches since load. */
+enum { SV_KERNEL_ROW_STATS = 0, SV_KERNEL_SAMPLE = 1, SV_KERNEL_SCHEDULE = 2, SV_NUM_KERNELS = 3 };
+void sv_profile_enable(int on);
+sv_status sv_profile_collect(double* total_ms, int64_t* launches);
+int64_t sv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SV_H_ */

@@ -1,0 +1,120 @@
+// Internal declarations shared by libsv's translation units (host and device).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/sv.h"
+
+namespace sv {
+
+// ---- row_stats kernel geometry ---------------------------------------------------------------
+constexpr int kStageBytes = 16384;     // one vocabulary chunk per pipeline stage
+constexpr int kStages = 4;             // bulk-copy ring depth
+constexpr int kConsumerWarps = 8;      // warps that reduce a chunk
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kStatsThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;  // 16-byte vectors per thread
+static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split");
+
+// ---- sample kernel geometry ------------------------------------------------------------------
+constexpr int kSampleThreads = 256;
+
+// Per-(row, chunk) statistics written by row_stats.
+struct alignas(16) ChunkRecord {
+  float m;     // max logit in the chunk
+  float s;     // sum of 2^((x - m) * log2(e) / T) over the chunk (0 for greedy rows)
+  int32_t g;   // first argmax in the chunk (vocabulary index), greedy rows only
+  float xval;  // logit at the row's drafted token, when that token lies in the chunk
+};
+
+// Per-row statistics merged over chunks by the request's combine step.
+struct alignas(16) RowStat {
+  double s;    // sum of 2^((x - m) * k) over the row
+  float m;     // row max
+  int32_t g;   // first argmax (greedy)
+};
+
+// Per-request state handed from row_stats' combine step to the sample kernel.
+enum : int32_t { kModeNone = 0, kModeBonus = 1, kModeResidual = 2 };
+struct alignas(16) ReqState {
+  int32_t mode;
+  int32_t a;          // accepted length == position of the draw
+  int64_t row_t;      // absolute target row index of row a
+  int64_t row_d;      // absolute draft row index of row a (residual mode)
+  float kscale;       // log2(e) / T, rounded to float
+  float mt, md;       // row maxima
+  float inv_st, inv_sd;  // 1 / row sums (float)
+  int32_t rec_row_t;  // record row index (request-major) of the target row a
+  double st;          // target row a's sum (double)
+  double u;           // u' for the draw
+  int32_t flags;
+  int32_t pad;
+};
+
+struct VerifyParams {
+  const void* target;
+  int64_t t_row_stride;     // elements
+  const int32_t* t_off;     // [B+1] or null => i * (Kmax + 1)
+  const void* draft;
+  int64_t d_row_stride;
+  const int32_t* d_off;     // [B+1] or null => i * Kmax
+  const int32_t* tokens;    // [B, tok_stride] or null => draft argmax (greedy only)
+  int32_t tok_stride;
+  const int32_t* keep_len;  // [B] or null => Kmax
+  const float* temperature; // [B] or null => greedy
+  const int32_t* request_ids;
+  uint64_t seed;
+  uint32_t round;
+  int32_t B, Kmax, V;
+  int32_t chunk_len, nchunks;  // vocabulary tiling
+  int32_t rows_per_req;        // 2 * Kmax + 1 record rows per request
+  // outputs
+  int32_t* out_tokens;      // [B, Kmax+1]
+  int32_t* out_accept_len;  // [B]
+  float* out_p;             // [B, Kmax] nullable
+  float* out_q;
+  uint8_t* out_flags;       // [B] nullable
+  // workspace
+  uint32_t* status;
+  uint32_t* cnt_stats;      // [B]
+  uint32_t* cnt_sample;     // [B]
+  ChunkRecord* rec;         // [B * rows_per_req * nchunks]
+  RowStat* rowstat;         // [B * rows_per_req]
+  ReqState* req;            // [B]
+  float* mass;              // [B * nchunks]
+};
+
+struct ScheduleParams {
+  const float* alpha;
+  int32_t alpha_stride;
+  const int32_t* draft_len;
+  int32_t B, Dmax;
+  double cost_a, cost_b;
+  int32_t budget;
+  int32_t n_ratios;
+  float ratios[8];
+  int32_t objective;
+  int32_t sort_size;  // power of two >= B * Dmax (or 1)
+  int32_t* out_keep_len;
+  int32_t* out_row_offsets;
+  int32_t* out_total_K;
+  int64_t* out_utility_q48;
+  uint32_t* status;
+};
+
+// Workspace layout for SV_OP_VERIFY.
+struct VerifyLayout {
+  size_t status, cnt_stats, cnt_sample, rec, rowstat, req, mass, total;
+};
+VerifyLayout verify_layout(int B, int Kmax, int nchunks);
+void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);
+
+// Launchers (return cudaError_t as int to keep CUDA headers out of this file).
+int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream);
+int launch_schedule(const ScheduleParams& p, void* stream);
+
+// Instrumentation hooks implemented in sv_api.cu.
+void prof_before(int kernel_id, void* stream);
+void prof_after(int kernel_id, void* stream);
+
+}  // namespace sv

@@ -1,0 +1,69 @@
+"""Shared helpers for the GPU parity tests: move a synthetic batch to the device, run the
+library through its C ABI, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import speculative_decoding_verification_74_gb300 as sv
+from oracle.verify import verify_batch, NEAR_PICK
+
+P_TOL = 1e-5   # absolute tolerance on reported probabilities (the stated contract)
+
+
+def dev_rows(rows: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(rows).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(rows, dtype=np.float32)).to(device)
+
+
+def i32(a, device="cuda"):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def f32(a, device="cuda"):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def run_ragged(b, ws=None, keep_len=None, want_pq=True):
+    """Run sv_verify_ragged on a synth VerifyBatch; returns numpy outputs."""
+    kl = b.keep_len if keep_len is None else keep_len
+    out = sv.verify_ragged(dev_rows(b.target, b.dtype), i32(b.t_offsets),
+                           dev_rows(b.draft, b.dtype) if b.draft is not None else None,
+                           i32(b.d_offsets) if b.draft is not None else None,
+                           i32(b.tokens), i32(kl), f32(b.temperature), b.Kmax, seed=b.seed, round_=b.round,
+                           request_ids=i32(b.request_ids), ws=ws, want_pq=want_pq)
+    torch.cuda.synchronize()
+    return tuple(None if o is None else o.cpu().numpy() for o in out)
+
+
+def oracle(b, keep_len=None):
+    kl = b.keep_len if keep_len is None else keep_len
+    return verify_batch(b.target, b.t_offsets, b.draft, b.d_offsets, b.tokens, kl, b.temperature, b.seed,
+                        b.round, b.request_ids, b.dtype, b.Kmax)
+
+
+def compare(orc, tok, alen, p=None, q=None, keep_len=None, temps=None, requests=None):
+    """Tokens and accepted lengths bit-exact up to the first near-boundary decision the oracle
+    reports (|u - p/q| < 1e-6, or an inverse-CDF pick within 1e-6 Z of a bin edge); p, q within
+    P_TOL.  Returns the number of requests whose comparison stopped at a near-boundary decision."""
+    B = len(alen)
+    near = 0
+    idx = range(B) if requests is None else requests
+    for i in idx:
+        npos = int(orc["near_pos"][i])
+        if npos < 0:
+            assert alen[i] == orc["accept_len"][i], (i, alen[i], orc["accept_len"][i])
+            assert np.array_equal(tok[i], orc["tokens"][i]), (i, tok[i], orc["tokens"][i])
+        else:
+            near += 1
+            assert np.array_equal(tok[i, :npos], orc["tokens"][i, :npos]), i
+            if orc["near_kind"][i] == NEAR_PICK:
+                assert alen[i] == orc["accept_len"][i], i
+        if p is not None and keep_len is not None:
+            n = int(keep_len[i])
+            if n:
+                assert np.allclose(p[i, :n], orc["p"][i, :n], atol=P_TOL, rtol=0), (i, p[i, :n], orc["p"][i, :n])
+                assert np.allclose(q[i, :n], orc["q"][i, :n], atol=P_TOL, rtol=0), (i, q[i, :n], orc["q"][i, :n])
+            assert np.all(np.isnan(p[i, n:])) and np.all(np.isnan(q[i, n:]))
+    return near
