@@ -255,24 +255,38 @@ def run_gpu(args, rank, world, local_rank):
     tot_pos = sum(pos[j % len(pos)] for j in range(warm, warm + steps))
     tot_bytes = sum(byts[j % len(byts)] for j in range(warm, warm + steps))
 
+    # every step is captured once per input set into a CUDA graph (kernels, no host work), so the
+    # timed loop measures the GPU, not the Python/ctypes launch path
     stream = torch.cuda.current_stream()
-    for j in range(warm):
+    for j in range(len(gw.sets)):
         gw.step(j)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    graphs, glaunch = [], []
+    for j in range(len(gw.sets)):
+        g = torch.cuda.CUDAGraph()
+        n0 = sv.sv_launch_count()
+        with torch.cuda.graph(g, stream=cap):
+            gw.step(j)
+        glaunch.append(sv.sv_launch_count() - n0)
+        graphs.append(g)
+    R = len(graphs)
+    for j in range(warm):
+        graphs[j % R].replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clocks = ClockSampler(local_rank) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
-    launches0 = sv.sv_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ev0.record(stream)
     for j in range(warm, warm + steps):
-        gw.step(j)
+        graphs[j % R].replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
-    launches = sv.sv_launch_count() - launches0
+    launches = sum(glaunch[j % R] for j in range(warm, warm + steps))
     clk = clocks.stop() if clocks else None
     if dist:
         t = torch.tensor([ms], device=dev)
@@ -280,13 +294,29 @@ def run_gpu(args, rank, world, local_rank):
         ms = float(t.item())
         dist.barrier()
 
-    # per-kernel durations: an instrumented repeat of the same K steps (CUDA events on the
-    # launching stream around every library kernel)
-    sv.sv_profile_enable(True)
-    for j in range(warm, warm + steps):
-        gw.step(j)
-    kms, kn = sv.sv_profile_collect()
-    sv.sv_profile_enable(False)
+    # per-kernel durations: the same K steps replayed from graphs captured with the library's
+    # CUDA-event brackets around each kernel (one graph at a time, collected after each replay)
+    kms = [0.0] * sv.SV_NUM_KERNELS
+    kn = [0] * sv.SV_NUM_KERNELS
+    for j0 in range(R):
+        idx = [j for j in range(warm, warm + steps) if j % R == j0]
+        if not idx:
+            continue
+        sv.sv_profile_reset()
+        sv.sv_profile_enable(True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            gw.step(j0)
+        sv.sv_profile_enable(False)
+        g.replay()          # warm replay (not counted)
+        torch.cuda.synchronize()
+        for _ in idx:
+            g.replay()
+            a, n = sv.sv_profile_collect()
+            kms = [x + y for x, y in zip(kms, a)]
+            kn = [x + y for x, y in zip(kn, n)]
+        sv.sv_profile_reset()
+        del g
 
     # end to end through host buffers: H2D of the step's inputs from pinned memory, the C ABI
     # call, D2H of the emitted tokens and accepted lengths
@@ -317,12 +347,13 @@ def run_gpu(args, rank, world, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
                      "avg_launch_us": k1_avg_ms * 1e3, "bytes_per_launch": k1_bytes,
-                     "timing": "CUDA events around each row_stats launch, instrumented repeat of the K steps"},
+                     "timing": "CUDA events around each row_stats launch inside graph replays of the same K steps"},
         "kernels_us_per_step": {sv.KERNEL_NAMES[i]: kms[i] * 1e3 / steps for i in range(sv.SV_NUM_KERNELS)
                                 if kn[i]},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": launches,
+        "timed_loop": "one CUDA graph per input set (captured C ABI calls), replayed K times",
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -22,6 +22,7 @@
  * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy
  *           default stream).  All work is enqueued asynchronously; no call
  *           synchronizes, except sv_query_status and sv_profile_collect.
+ *           Every call may be captured into a CUDA graph.
  * Errors    Every call returns an sv_status.  Host-side checks (NULL
  *           pointers, sizes, alignment, workspace size) return before any
  *           work is enqueued.  Values that only the device sees (token ids,
@@ -32,9 +33,10 @@
  *           The kernels never trap; every wait in them is bounded.
  * Logits    Rows of V logits, contiguous, bf16 (SV_BF16) or float32
  *           (SV_F32), finite or -inf (a masked token).  NaN and +inf are not
- *           valid logits (results unspecified).  Row starts must be 16-byte
- *           aligned: the base pointer 16-byte aligned and the row stride (in
- *           elements) times the element size a multiple of 16.
+ *           valid logits (results unspecified).  The row stride (elements) is
+ *           at least V; rows may start at any element (the 16-byte aligned
+ *           interior of each row is bulk-copied, the few elements outside it
+ *           are loaded one by one), so no byte outside a row is read.
  * Randomness  The accept test and the resampling draw use Philox4x32-10
  *           (Salmon et al., SC'11) with key = (seed low, seed high word) and
  *           counter = (position, request id, purpose, round); purpose 0 is the
@@ -223,13 +225,17 @@ const char* sv_status_string(sv_status s);
 const char* sv_last_error_string(void);
 
 /* Instrumentation.  While enabled, every library kernel launch is bracketed by
- * CUDA events on its stream.  sv_profile_collect synchronizes the device, adds
- * the elapsed times per kernel id into total_ms[id] and the launch counts into
- * launches[id] (arrays of SV_NUM_KERNELS), and forgets the recorded events.
- * sv_launch_count returns the number of library kernel launches since load. */
+ * CUDA events on its stream (recorded into the graph when the stream is being
+ * captured, so a graph replay re-records them).  sv_profile_collect
+ * synchronizes the device and adds, for every bracket recorded since the last
+ * sv_profile_reset, its elapsed time to total_ms[kernel id] and 1 to
+ * launches[kernel id] (arrays of SV_NUM_KERNELS).  sv_profile_reset forgets the
+ * brackets.  sv_launch_count returns the number of library kernel launches (or
+ * captured launch nodes) since the library was loaded. */
 enum { SV_KERNEL_ROW_STATS = 0, SV_KERNEL_SAMPLE = 1, SV_KERNEL_SCHEDULE = 2, SV_NUM_KERNELS = 3 };
 void sv_profile_enable(int on);
 sv_status sv_profile_collect(double* total_ms, int64_t* launches);
+void sv_profile_reset(void);
 int64_t sv_launch_count(void);
 
 #ifdef __cplusplus

@@ -51,6 +51,7 @@ _SIGS = {
     "sv_last_error_string": (_c.c_char_p, []),
     "sv_profile_enable": (None, [_c.c_int]),
     "sv_profile_collect": (_c.c_int, [_c.POINTER(_c.c_double), _c.POINTER(_i64)]),
+    "sv_profile_reset": (None, []),
     "sv_launch_count": (_i64, []),
 }
 
@@ -182,6 +183,10 @@ def sv_profile_collect() -> tuple[list[float], list[int]]:
     return list(ms), list(n)
 
 
+def sv_profile_reset() -> None:
+    lib().sv_profile_reset()
+
+
 def sv_launch_count() -> int:
     return int(lib().sv_launch_count())
 
@@ -200,6 +205,8 @@ def workspace(op: int, B: int, Kmax: int, V: int, dt: int, device="cuda") -> tor
 
 def _rows(x: torch.Tensor):
     """(base tensor, row stride) for [..., V] logits with a contiguous last dimension."""
+    if x.numel() == 0:
+        return x, x.shape[-1]
     if x.stride(-1) != 1:
         raise ValueError("logit rows must be contiguous")
     return x, (x.stride(-2) if x.dim() >= 2 else x.shape[-1])

@@ -28,15 +28,12 @@ sv_status cuda_fail(int e, const char* what) {
   return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(e)));
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int elt_size(sv_dtype dt) { return dt == SV_BF16 ? 2 : 4; }
 
 sv_status check_rows(const char* name, const void* base, int64_t stride, int V, sv_dtype dt) {
-  if (!aligned16(base)) return fail(SV_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  if ((reinterpret_cast<uintptr_t>(base) % elt_size(dt)) != 0)
+    return fail(SV_ERR_INVALID_ARG, "%s is not aligned to its element size", name);
   if (stride < V) return fail(SV_ERR_INVALID_ARG, "%s row stride %lld < V %d", name, (long long)stride, V);
-  if ((stride * elt_size(dt)) % 16 != 0)
-    return fail(SV_ERR_INVALID_ARG, "%s row stride (%lld elements) is not a multiple of 16 bytes", name,
-                (long long)stride);
   return SV_OK;
 }
 
@@ -116,12 +113,26 @@ sv_status check_common(const void* target, int64_t t_row_stride, const void* dra
 // =============================================================================================
 // sv:: hooks used by the kernels' launchers
 // =============================================================================================
+namespace {
+// Inside a stream capture the bracket must become an event-record node of the graph (external
+// record) so that every replay re-records it and its elapsed time can be read.
+void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+}  // namespace
+
 namespace sv {
+bool prof_enabled() { return g_prof_on; }
 void prof_before(int id, void* stream) {
   if (!g_prof_on) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   cudaEvent_t a = take_event();
-  cudaEventRecord(a, static_cast<cudaStream_t>(stream));
+  record(a, static_cast<cudaStream_t>(stream));
   g_pending_start[id] = a;
 }
 void prof_after(int id, void* stream) {
@@ -129,7 +140,7 @@ void prof_after(int id, void* stream) {
   if (!g_prof_on) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   cudaEvent_t b = take_event();
-  cudaEventRecord(b, static_cast<cudaStream_t>(stream));
+  record(b, static_cast<cudaStream_t>(stream));
   g_prof.push_back({id, g_pending_start[id], b});
 }
 }  // namespace sv
@@ -346,11 +357,17 @@ sv_status sv_profile_collect(double* total_ms, int64_t* launches) {
       total_ms[r.id] += ms;
       launches[r.id] += 1;
     }
+  }
+  return SV_OK;
+}
+
+void sv_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const ProfRec& r : g_prof) {
     g_event_pool.push_back(r.a);
     g_event_pool.push_back(r.b);
   }
   g_prof.clear();
-  return SV_OK;
 }
 
 int64_t sv_launch_count(void) { return g_launches.load(); }

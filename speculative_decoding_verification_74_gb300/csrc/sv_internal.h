@@ -114,6 +114,7 @@ int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream
 int launch_schedule(const ScheduleParams& p, void* stream);
 
 // Instrumentation hooks implemented in sv_api.cu.
+bool prof_enabled();
 void prof_before(int kernel_id, void* stream);
 void prof_after(int kernel_id, void* stream);
 

@@ -69,6 +69,20 @@ __device__ __forceinline__ const char* row_ptr(const void* base, int64_t row, in
   return reinterpret_cast<const char*>(base) + row * stride * kElt;
 }
 
+// A chunk [c0, c0 + len) of a row split into a head of plain loads, a 16-byte aligned interior of
+// nvec vectors (bulk-copied) and a tail of plain loads; rows may start at any element.
+struct ChunkSplit {
+  int head, nvec, tail;
+};
+template <int kElt>
+__device__ __forceinline__ ChunkSplit split_chunk(const char* row, int c0, int len) {
+  const uintptr_t s = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(c0) * kElt;
+  const uintptr_t e = s + static_cast<uintptr_t>(len) * kElt;
+  const uintptr_t a = (s + 15u) & ~uintptr_t(15), z = e & ~uintptr_t(15);
+  if (z <= a) return ChunkSplit{len, 0, 0};
+  return ChunkSplit{static_cast<int>((a - s) / kElt), static_cast<int>((z - a) / 16), static_cast<int>((e - z) / kElt)};
+}
+
 __device__ __forceinline__ ChunkRecord ld_record(const ChunkRecord* r) {
   const float4 v = __ldcg(reinterpret_cast<const float4*>(r));
   ChunkRecord o;
@@ -95,8 +109,8 @@ __device__ uint16_t request_info(const VerifyParams& p, int i, uint32_t* bad_out
   if (n < 0 || n > p.Kmax) bad |= SV_DEV_BAD_KEEP_LEN;
   if (!(T >= 0.0f) || isinf(T)) bad |= SV_DEV_BAD_TEMPERATURE;
   const bool sampled = T > 0.0f;
-  const bool need_draft = sampled || p.tokens == nullptr;
-  if (sampled && p.tokens == nullptr) bad |= SV_DEV_BAD_TOKEN;
+  const bool need_draft = (sampled || p.tokens == nullptr) && n > 0;  // n == 0: bonus row only
+  if (sampled && n > 0 && p.tokens == nullptr) bad |= SV_DEV_BAD_TOKEN;
   if (need_draft && p.draft == nullptr) bad |= SV_DEV_NO_DRAFT_ROWS;
   if (!bad && p.t_off && (__ldg(p.t_off + i + 1) - __ldg(p.t_off + i) < n + 1 || __ldg(p.t_off + i) < 0))
     bad |= SV_DEV_BAD_OFFSETS;
@@ -343,14 +357,13 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
         const char* src = r <= Kmax ? row_ptr<DT>(p.target, row, p.t_row_stride)
                                     : row_ptr<DT>(p.draft, row, p.d_row_stride);
         const int c0 = c * p.chunk_len;
-        const int len = min(p.chunk_len, p.V - c0);
-        const uint32_t bytes = static_cast<uint32_t>(len * kElt) & ~15u;
-        if (bytes == 0) {
+        const ChunkSplit sp = split_chunk<kElt>(src, c0, min(p.chunk_len, p.V - c0));
+        if (sp.nvec == 0) {
           mbar_arrive(&full_bar[stage]);
         } else {
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          bulk_g2s(stages + stage * kStageBytes, src + static_cast<int64_t>(c0) * kElt, bytes,
-                   &full_bar[stage], pol);
+          mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(sp.nvec) * 16u);
+          bulk_g2s(stages + stage * kStageBytes, src + static_cast<int64_t>(c0 + sp.head) * kElt,
+                   static_cast<uint32_t>(sp.nvec) * 16u, &full_bar[stage], pol);
         }
       }
       // drain: every issued copy must land before the CTA may exit
@@ -390,8 +403,15 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 
     const int c0 = c * p.chunk_len;
     const int len = kind == kLoad ? min(p.chunk_len, p.V - c0) : 0;
-    const int nvec = (len * kElt) >> 4;
-    const int tail = len - nvec * kVec;
+    const char* rowp = nullptr;
+    if (kind == kLoad) {
+      const int64_t row = r <= Kmax ? target_row(p, i, r) : draft_row(p, i, r - Kmax - 1);
+      rowp = r <= Kmax ? row_ptr<DT>(p.target, row, p.t_row_stride) : row_ptr<DT>(p.draft, row, p.d_row_stride);
+    }
+    const ChunkSplit sp = kind == kLoad ? split_chunk<kElt>(rowp, c0, len) : ChunkSplit{0, 0, 0};
+    const int head = sp.head, nvec = sp.nvec, tail = sp.tail;
+    const int v0 = c0 + head;                      // vocabulary index of the first staged element
+    const int t0 = v0 + nvec * kVec;               // first tail element
 
     // A timed-out wait does not leave the loop here: every consumer thread must reach the same
     // named barriers; the abort decision is taken uniformly after them.
@@ -404,34 +424,31 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
       raw[j] = v < nvec ? lds128(sb + v * 16) : make_uint4(0, 0, 0, 0);
     }
     float xval = NAN;
-    if (tid == 0 && tok >= c0 && tok < c0 + nvec * kVec) {
+    if (tid == 0 && tok >= v0 && tok < t0) {
       if constexpr (DT == SV_BF16)
-        xval = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[tok - c0]) << 16);
+        xval = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[tok - v0]) << 16);
       else
-        xval = reinterpret_cast<const float*>(sb)[tok - c0];
+        xval = reinterpret_cast<const float*>(sb)[tok - v0];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
 
-    // tail elements (fewer than one vector) straight from global memory
-    float tail_x = 0.0f;
-    const bool has_tail = kind == kLoad && tid < tail;
-    const char* rowp = nullptr;
-    if (kind == kLoad && (tail > 0)) {
-      const int64_t row = r <= Kmax ? target_row(p, i, r) : draft_row(p, i, r - Kmax - 1);
-      rowp = r <= Kmax ? row_ptr<DT>(p.target, row, p.t_row_stride) : row_ptr<DT>(p.draft, row, p.d_row_stride);
-      if (has_tail) tail_x = load_logit<DT>(rowp, c0 + nvec * kVec + tid);
-      if (tid == 0 && tok >= c0 + nvec * kVec && tok < c0 + len) xval = load_logit<DT>(rowp, tok);
-    }
+    // head / tail elements outside the 16-byte aligned interior: plain loads
+    const bool has_head = tid < head, has_tail = tid < tail;
+    const float head_x = has_head ? load_logit<DT>(rowp, c0 + tid) : 0.0f;
+    const float tail_x = has_tail ? load_logit<DT>(rowp, t0 + tid) : 0.0f;
+    if (tid == 0 && kind == kLoad && tok >= c0 && tok < c0 + len && !(tok >= v0 && tok < t0))
+      xval = load_logit<DT>(rowp, tok);
 
     float m = -INFINITY, sacc = 0.0f;
     int g = -1;
     if (!sampled) {
+      if (has_head) { m = head_x; g = c0 + tid; }
 #pragma unroll
       for (int j = 0; j < kVecPerThread; ++j) {
         const int v = tid + j * kConsumerThreads;
         if (v < nvec) {
-          const int base = c0 + v * kVec;
+          const int base = v0 + v * kVec;
           if constexpr (DT == SV_BF16) {
             const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
           }
         }
       }
-      if (has_tail && (g < 0 || tail_x > m)) { m = tail_x; g = c0 + nvec * kVec + tid; }
+      if (has_tail && (g < 0 || tail_x > m)) { m = tail_x; g = t0 + tid; }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
@@ -469,8 +486,10 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
           }
         }
       }
+      if (has_head) m = fmaxf(m, head_x);
       if (has_tail) m = fmaxf(m, tail_x);
       if (m != -INFINITY) {
+        if (has_head) sacc += ex2_approx((head_x - m) * kscale);
 #pragma unroll
         for (int j = 0; j < kVecPerThread; ++j) {
           if (tid + j * kConsumerThreads < nvec) {
@@ -579,7 +598,7 @@ __device__ __forceinline__ float draw_weight(const unsigned char* tb, const unsi
 template <int DT>
 __device__ void stage_chunk(unsigned char* dst, const char* src, int len, int tid) {
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
-  const int nvec = (len * kElt) >> 4;
+  const int nvec = (reinterpret_cast<uintptr_t>(src) & 15u) ? 0 : ((len * kElt) >> 4);
   for (int v = tid; v < nvec; v += kSampleThreads)
     reinterpret_cast<uint4*>(dst)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
   for (int e = nvec * (16 / kElt) + tid; e < len; e += kSampleThreads) {
@@ -799,7 +818,9 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // Programmatic dependent launch lets the sample grid's launch overlap the row_stats tail; it
+  // is left out while instrumentation puts an event between the two kernels.
+  cfg.numAttrs = prof_enabled() ? 0 : 1;
   prof_before(SV_KERNEL_SAMPLE, stream);
   e = cudaLaunchKernelEx(&cfg, sample_kernel<DT>, p);
   prof_after(SV_KERNEL_SAMPLE, stream);

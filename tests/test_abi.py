@@ -56,11 +56,11 @@ def test_workspace_sizes(L):
 def test_host_validation_without_gpu(L):
     INV, WS = sv.SV_ERR_INVALID_ARG, sv.SV_ERR_WORKSPACE
     fake = 1 << 20          # an aligned, never-dereferenced address
-    # greedy: NULL target, bad sizes, misaligned rows, no draft information
+    # greedy: NULL target, bad sizes, rows not aligned to the element size, no draft information
     assert L.sv_verify_greedy(None, 100, None, 0, fake, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
     assert L.sv_verify_greedy(fake, 100, None, 0, fake, 0, 4, -1, 100, fake, fake, fake, 1 << 20, None) == INV
-    assert L.sv_verify_greedy(fake + 2, 104, None, 0, fake, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
-    assert L.sv_verify_greedy(fake, 101, None, 0, fake, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
+    assert L.sv_verify_greedy(fake + 1, 104, None, 0, fake, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
+    assert L.sv_verify_greedy(fake + 2, 104, None, 0, fake, 1, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
     assert L.sv_verify_greedy(fake, 99, None, 0, fake, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
     assert L.sv_verify_greedy(fake, 104, None, 0, None, 0, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
     assert L.sv_verify_greedy(fake, 104, None, 0, fake, 7, 4, 3, 100, fake, fake, fake, 1 << 20, None) == INV
