@@ -27,8 +27,8 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, S
 SV_BF16, SV_F32 = 0, 1
 SV_OP_VERIFY, SV_OP_SCHEDULE = 0, 1
 SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
-SV_KERNEL_ROW_STATS, SV_KERNEL_SAMPLE, SV_KERNEL_SCHEDULE, SV_NUM_KERNELS = 0, 1, 2, 3
-KERNEL_NAMES = ("row_stats", "sample", "schedule")
+SV_KERNEL_ROW_STATS, SV_KERNEL_FINALIZE, SV_KERNEL_SCHEDULE, SV_NUM_KERNELS = 0, 1, 2, 3
+KERNEL_NAMES = ("row_stats", "finalize", "schedule")
 
 _c = ctypes
 _vp, _i32, _i64, _u32, _u64, _f32, _sz = (_c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_uint64,

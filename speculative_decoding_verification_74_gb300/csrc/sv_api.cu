@@ -81,12 +81,10 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
   p.nchunks = nc;
   p.rows_per_req = 2 * p.Kmax + 1;
   p.status = reinterpret_cast<uint32_t*>(w + L.status);
-  p.cnt_stats = reinterpret_cast<uint32_t*>(w + L.cnt_stats);
   p.cnt_sample = reinterpret_cast<uint32_t*>(w + L.cnt_sample);
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
-  p.rowstat = reinterpret_cast<sv::RowStat*>(w + L.rowstat);
-  p.req = reinterpret_cast<sv::ReqState*>(w + L.req);
   p.mass = reinterpret_cast<float*>(w + L.mass);
+  p.wmass = reinterpret_cast<float*>(w + L.wmass);
   const int e = sv::launch_verify(p, dt, sampled, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;

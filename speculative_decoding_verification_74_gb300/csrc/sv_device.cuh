@@ -103,14 +103,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase completes (or the
+// hint, in ns, runs out) instead of spinning and taking issue slots from working warps.
+constexpr uint32_t kSuspendHintNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -123,23 +126,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kWaitMaxPolls = 1u << 24;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1; it < kWaitMaxPolls; ++it) {
+  // a few quick polls, then back off with nanosleep so a waiting warp takes few issue slots;
+  // the timer is read only once a wait runs long
+  for (uint32_t it = 0; it < 4; ++it)
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 4; it < kWaitMaxPolls; ++it) {
+    __nanosleep(it < 64 ? 32 : 256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
   atomicOr(status, SV_DEV_TIMEOUT);
   return false;
 }
+// Philox uniform as float (exact: 24 significant bits).
+__device__ __forceinline__ float philox_uniform_f(uint64_t seed, uint32_t position, uint32_t request,
+                                                  uint32_t purpose, uint32_t round) {
+  return static_cast<float>(philox_word0(position, request, purpose, round, seed) >> 8) * (1.0f / 16777216.0f);
+}
 // 1-D bulk copy global -> shared, completion signalled on `bar` with `bytes` transaction bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {

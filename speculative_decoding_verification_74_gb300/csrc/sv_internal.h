@@ -18,6 +18,7 @@ static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split
 
 // ---- sample kernel geometry ------------------------------------------------------------------
 constexpr int kSampleThreads = 256;
+constexpr int kSampleWarps = kSampleThreads / 32;
 
 // Per-(row, chunk) statistics written by row_stats.
 struct alignas(16) ChunkRecord {
@@ -27,14 +28,7 @@ struct alignas(16) ChunkRecord {
   float xval;  // logit at the row's drafted token, when that token lies in the chunk
 };
 
-// Per-row statistics merged over chunks by the request's combine step.
-struct alignas(16) RowStat {
-  double s;    // sum of 2^((x - m) * k) over the row
-  float m;     // row max
-  int32_t g;   // first argmax (greedy)
-};
-
-// Per-request state handed from row_stats' combine step to the sample kernel.
+// What the draw at the accepted length needs (kept in shared memory by the finalize kernel).
 enum : int32_t { kModeNone = 0, kModeBonus = 1, kModeResidual = 2 };
 struct alignas(16) ReqState {
   int32_t mode;
@@ -45,10 +39,9 @@ struct alignas(16) ReqState {
   float mt, md;       // row maxima
   float inv_st, inv_sd;  // 1 / row sums (float)
   int32_t rec_row_t;  // record row index (request-major) of the target row a
-  double st;          // target row a's sum (double)
-  double u;           // u' for the draw
+  float st;           // target row a's sum
+  float u;            // u' for the draw
   int32_t flags;
-  int32_t pad;
 };
 
 struct VerifyParams {
@@ -76,12 +69,10 @@ struct VerifyParams {
   uint8_t* out_flags;       // [B] nullable
   // workspace
   uint32_t* status;
-  uint32_t* cnt_stats;      // [B]
-  uint32_t* cnt_sample;     // [B]
+  uint32_t* cnt_sample;     // [B] per-request counter of the draw's chunk CTAs
   ChunkRecord* rec;         // [B * rows_per_req * nchunks]
-  RowStat* rowstat;         // [B * rows_per_req]
-  ReqState* req;            // [B]
-  float* mass;              // [B * nchunks]
+  float* mass;              // [B * nchunks] residual mass per chunk
+  float* wmass;             // [B * nchunks * kSampleWarps] residual mass per warp range
 };
 
 struct ScheduleParams {
@@ -104,7 +95,7 @@ struct ScheduleParams {
 
 // Workspace layout for SV_OP_VERIFY.
 struct VerifyLayout {
-  size_t status, cnt_stats, cnt_sample, rec, rowstat, req, mass, total;
+  size_t status, cnt_sample, rec, mass, wmass, total;
 };
 VerifyLayout verify_layout(int B, int Kmax, int nchunks);
 void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);

@@ -2,21 +2,26 @@
 //
 // row_stats  One streaming pass over every logit row a round needs.  A persistent grid walks
 //            (request, row, vocabulary chunk) tasks in request-major order; per CTA one
-//            producer lane issues 1-D bulk copies (cp.async.bulk) of 16 KB chunks into a
-//            4-stage shared-memory ring and eight consumer warps reduce each chunk to
-//            {max, sum 2^((x-max) log2(e)/T), first argmax, logit at the drafted token}.
-//            The CTA that finishes a request's last chunk (atomic counter, no waiting)
-//            merges its chunks and runs the accept chain: the greedy test x_k == argmax,
-//            or the rejection test u_k q_k(x_k) < p_k(x_k), first rejection = accepted
-//            length (AngelSpec explainer, "MTP: fix position 2 and 3", eq. L_e2e: one
-//            rejection voids every later position; AngelSpec release article, "Why one
-//            universal drafter underperforms": rejection-sampling verification in one pass).
-// sample     For sampled requests: the draw at the accepted length a, from
-//            norm(max(0, p_a - q_a)) after a rejection or from p_n when every drafted token
-//            was accepted (the bonus row), by inverse CDF in vocabulary order.  Residual
-//            requests re-read their two rows once (chunk sums, then a scan of the chunk that
-//            holds the crossing); bonus requests reuse row_stats' chunk sums and scan one
-//            chunk.
+//            producer lane issues 1-D bulk copies (cp.async.bulk) of <= 16 KB chunks into a
+//            4-stage shared-memory ring and eight consumer warps reduce each chunk to a record
+//            {max, sum 2^((x-max) log2(e)/T), first argmax, logit at the drafted token}.  The
+//            kernel only streams and writes records: no atomics, no fences, no waiting on other
+//            CTAs.
+// finalize   Launched behind row_stats with programmatic dependent launch, grid (chunks, B).
+//            Every CTA of request i merges the request's records into row statistics in shared
+//            memory and runs the accept chain: the greedy test x_k == argmax, or the rejection
+//            test u_k q_k(x_k) < p_k(x_k), first rejection = accepted length (AngelSpec
+//            explainer, "MTP: fix position 2 and 3", eq. L_e2e: one rejection voids every later
+//            position; AngelSpec release article, "Why one universal drafter underperforms":
+//            rejection-sampling verification in one pass).  The CTAs agree without
+//            communicating (same inputs, same reduction order); CTA 0 writes the outputs.
+//            Sampled requests then draw the token at the accepted length a, from
+//            norm(max(0, p_a - q_a)) after a rejection or from p_n when every drafted token was
+//            accepted (the bonus row), by inverse CDF in vocabulary order.  After a rejection
+//            each CTA sums the residual over its chunk (per chunk and per warp range) and the
+//            request's last CTA (one acquire-release counter) finds the crossing chunk, the
+//            crossing range, and scans ~1/8 of one chunk with one warp.  Bonus requests reuse
+//            row_stats' chunk sums and recompute one chunk.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,7 +33,7 @@
 namespace sv {
 namespace {
 
-constexpr double kLog2e = 1.4426950408889634074;
+constexpr float kLog2eF = 1.44269504088896340736f;
 
 // request info, one uint16 per request, cached in shared memory by every row_stats CTA
 constexpr uint16_t kInfoN = 0x3FF;
@@ -36,24 +41,13 @@ constexpr uint16_t kInfoNeedDraft = 1u << 10;
 constexpr uint16_t kInfoSampled = 1u << 11;
 constexpr uint16_t kInfoInvalid = 1u << 12;
 
-enum : int { kSkip = 0, kLoad = 1, kDummy = 2 };
+// log2(e) / T in float; every kernel uses this one value for a request's temperature.
+__device__ __forceinline__ float kscale_of(float T) { return __fdiv_rn(kLog2eF, T); }
 
-__device__ __forceinline__ float kscale_of(float T) {
-  return static_cast<float>(kLog2e / static_cast<double>(T));
-}
-
-__device__ __forceinline__ int slot_kind(uint16_t info, int r, int c, int Kmax) {
-  if (info & kInfoInvalid) return (r == 0 && c == 0) ? kDummy : kSkip;
-  const int n = info & kInfoN;
-  if (r <= Kmax) return r <= n ? kLoad : kSkip;
-  return ((info & kInfoNeedDraft) && (r - Kmax - 1) < n) ? kLoad : kSkip;
-}
-
-__device__ __forceinline__ uint32_t expected_tasks(uint16_t info, int nchunks) {
-  if (info & kInfoInvalid) return 1u;
-  const uint32_t n = info & kInfoN;
-  const uint32_t rows = n + 1u + ((info & kInfoNeedDraft) ? n : 0u);
-  return rows * static_cast<uint32_t>(nchunks);
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ int64_t target_row(const VerifyParams& p, int i, int k) {
@@ -69,8 +63,8 @@ __device__ __forceinline__ const char* row_ptr(const void* base, int64_t row, in
   return reinterpret_cast<const char*>(base) + row * stride * kElt;
 }
 
-// A chunk [c0, c0 + len) of a row split into a head of plain loads, a 16-byte aligned interior of
-// nvec vectors (bulk-copied) and a tail of plain loads; rows may start at any element.
+// A range [c0, c0 + len) of a row split into a head of plain loads, a 16-byte aligned interior of
+// nvec vectors and a tail of plain loads; rows may start at any element.
 struct ChunkSplit {
   int head, nvec, tail;
 };
@@ -93,10 +87,13 @@ __device__ __forceinline__ ChunkRecord ld_record(const ChunkRecord* r) {
   return o;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
+// hi + lo += x with the rounding error of the addition carried in lo (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bb = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+  hi = s;
+  lo = __fadd_rn(lo, err);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -131,167 +128,60 @@ __device__ void write_invalid(const VerifyParams& p, int i, int tid, int nthread
   if (tid == 0) {
     p.out_accept_len[i] = -1;
     if (p.out_flags) p.out_flags[i] = SV_FLAG_INVALID;
-    p.req[i].mode = kModeNone;
   }
-}
-
-// ------------------------------------------------------------------------------------------
-// combine: merge a request's chunk records into row statistics, run the accept chain, emit.
-// Runs on the 256 consumer threads of the CTA that completed the request.
-// ------------------------------------------------------------------------------------------
-struct CombineSmem {
-  int a_min;
-  uint32_t flags;
-  uint32_t bad;
-};
-
-__device__ void combine_request(const VerifyParams& p, int i, uint16_t info, int tid, CombineSmem* cs) {
-  const int lane = tid & 31, warp = tid >> 5;
-  const int Kmax = p.Kmax, NC = p.nchunks, R = p.rows_per_req;
-  if (info & kInfoInvalid) {
-    write_invalid(p, i, tid, kConsumerThreads);
-    if (tid == 0) p.cnt_stats[i] = 0;
-    named_bar(1, kConsumerThreads);
-    return;
-  }
-  const int n = info & kInfoN;
-  const bool sampled = info & kInfoSampled;
-  const bool need_draft = info & kInfoNeedDraft;
-  const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
-  const float kscale = sampled ? kscale_of(T) : 0.0f;
-  const int nrows = n + 1 + (need_draft ? n : 0);
-  const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
-
-  // 1. row statistics
-  for (int q = warp; q < nrows; q += kConsumerWarps) {
-    const int r = q <= n ? q : Kmax + 1 + (q - n - 1);
-    const ChunkRecord* rr = p.rec + (static_cast<int64_t>(i) * R + r) * NC;
-    float m = -INFINITY;
-    int g = -1;
-    for (int c = lane; c < NC; c += 32) {
-      const ChunkRecord rc = ld_record(rr + c);
-      if (sampled) m = fmaxf(m, rc.m);
-      else merge_argmax(m, g, rc.m, rc.g);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const int g2 = __shfl_xor_sync(0xFFFFFFFFu, g, o);
-      if (sampled) m = fmaxf(m, m2);
-      else merge_argmax(m, g, m2, g2);
-    }
-    double s = 0.0;
-    if (sampled && m != -INFINITY) {
-      for (int c = lane; c < NC; c += 32) {
-        const ChunkRecord rc = ld_record(rr + c);
-        if (rc.m != -INFINITY) s += static_cast<double>(rc.s) * static_cast<double>(exp2f((rc.m - m) * kscale));
-      }
-      s = warp_sum_d(s);
-    }
-    if (lane == 0) {
-      RowStat rs;
-      rs.s = s;
-      rs.m = m;
-      rs.g = g;
-      p.rowstat[static_cast<int64_t>(i) * R + r] = rs;
-    }
-  }
-  if (tid == 0) {
-    cs->a_min = n;
-    cs->flags = 0;
-    cs->bad = 0;
-  }
-  named_bar(1, kConsumerThreads);
-
-  // 2. accept tests (each position independently; the first rejection is a min-reduction)
-  const RowStat* rs = p.rowstat + static_cast<int64_t>(i) * R;
-  for (int k = tid; k < n; k += kConsumerThreads) {
-    const int x = p.tokens ? __ldg(p.tokens + static_cast<int64_t>(i) * p.tok_stride + k) : rs[Kmax + 1 + k].g;
-    bool acc;
-    double pv, qv;
-    if (x < 0 || x >= p.V) {
-      atomicOr(&cs->bad, SV_DEV_BAD_TOKEN);
-      acc = false;
-      pv = qv = NAN;
-    } else if (!sampled) {
-      acc = (x == rs[k].g);
-      pv = acc ? 1.0 : 0.0;
-      qv = 1.0;
-    } else {
-      const int cx = x / p.chunk_len;
-      const float xt = ld_record(p.rec + (static_cast<int64_t>(i) * R + k) * NC + cx).xval;
-      const float xd = ld_record(p.rec + (static_cast<int64_t>(i) * R + Kmax + 1 + k) * NC + cx).xval;
-      const RowStat rt = rs[k], rd = rs[Kmax + 1 + k];
-      pv = exp2(static_cast<double>(xt - rt.m) * static_cast<double>(kscale)) / rt.s;
-      qv = exp2(static_cast<double>(xd - rd.m) * static_cast<double>(kscale)) / rd.s;
-      const double u = philox_uniform(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 0u, p.round);
-      acc = u * qv < pv;
-      if (qv == 0.0) atomicOr(&cs->flags, SV_FLAG_Q_ZERO);
-    }
-    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = static_cast<float>(pv);
-    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = static_cast<float>(qv);
-    if (!acc) atomicMin(&cs->a_min, k);
-  }
-  for (int k = n + tid; k < Kmax; k += kConsumerThreads) {
-    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
-    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
-  }
-  named_bar(1, kConsumerThreads);
-
-  // 3. emit
-  if (cs->bad) {
-    if (tid == 0) atomicOr(p.status, cs->bad);
-    write_invalid(p, i, tid, kConsumerThreads);
-  } else {
-    const int a = cs->a_min;
-    for (int j = tid; j <= Kmax; j += kConsumerThreads) {
-      int v = -1;
-      if (j < a) v = p.tokens ? __ldg(p.tokens + static_cast<int64_t>(i) * p.tok_stride + j) : rs[Kmax + 1 + j].g;
-      else if (j == a && !sampled) v = rs[a].g;
-      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
-    }
-    if (tid == 0) {
-      p.out_accept_len[i] = a;
-      if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(cs->flags);
-      ReqState st;
-      st.mode = kModeNone;
-      st.a = a;
-      st.flags = static_cast<int32_t>(cs->flags);
-      st.pad = 0;
-      if (sampled) {
-        st.mode = a < n ? kModeResidual : kModeBonus;
-        st.row_t = target_row(p, i, a);
-        st.row_d = a < n ? draft_row(p, i, a) : 0;
-        st.kscale = kscale;
-        st.mt = rs[a].m;
-        st.st = rs[a].s;
-        st.inv_st = static_cast<float>(1.0 / rs[a].s);
-        st.md = a < n ? rs[Kmax + 1 + a].m : 0.0f;
-        st.inv_sd = a < n ? static_cast<float>(1.0 / rs[Kmax + 1 + a].s) : 0.0f;
-        st.rec_row_t = i * R + a;
-        st.u = philox_uniform(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
-      } else {
-        st.row_t = st.row_d = 0;
-        st.kscale = st.mt = st.md = st.inv_st = st.inv_sd = 0.0f;
-        st.rec_row_t = 0;
-        st.st = st.u = 0.0;
-      }
-      p.req[i] = st;
-    }
-  }
-  if (tid == 0) p.cnt_stats[i] = 0;
-  named_bar(1, kConsumerThreads);
 }
 
 // ------------------------------------------------------------------------------------------
 // row_stats kernel
 // ------------------------------------------------------------------------------------------
+// Rows are numbered request by request (row_start[i] = first row of request i, built in every
+// CTA's prologue); inside a request its n_i + 1 target rows come first, then its n_i draft rows
+// when it reads them.  The (row, chunk) tasks are split into one contiguous range per CTA, so a
+// CTA keeps running per-thread statistics across consecutive chunks of a row and reduces across
+// threads only where a row ends.  The first chunk of each (CTA, row) piece receives the merged
+// record; the other chunks of the piece receive an empty record (max -inf) that still carries
+// the drafted token's logit when the token lies in that chunk.
+struct RowRef {
+  int i;        // request
+  int k;        // position inside the request
+  int rec_row;  // record row: k for target rows, Kmax + 1 + k for draft rows
+  bool is_target;
+};
+
+__device__ __forceinline__ void locate_row(const int* row_start, const uint16_t* info, int Kmax, int row, int& i,
+                                           RowRef& rr) {
+  while (row >= row_start[i + 1]) ++i;  // rows are visited in increasing order
+  const int q = row - row_start[i];
+  const int n = info[i] & kInfoN;
+  rr.i = i;
+  rr.is_target = q <= n;
+  rr.k = rr.is_target ? q : q - n - 1;
+  rr.rec_row = rr.is_target ? rr.k : Kmax + 1 + rr.k;
+}
+
+template <int DT>
+__device__ __forceinline__ const char* row_base(const VerifyParams& p, const RowRef& rr) {
+  return rr.is_target ? row_ptr<DT>(p.target, target_row(p, rr.i, rr.k), p.t_row_stride)
+                      : row_ptr<DT>(p.draft, draft_row(p, rr.i, rr.k), p.d_row_stride);
+}
+
+__device__ __forceinline__ int rows_of(uint16_t inf) {
+  if (inf & kInfoInvalid) return 0;
+  const int n = inf & kInfoN;
+  return n + 1 + ((inf & kInfoNeedDraft) ? n : 0);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 struct StatsRed {
   float m[kConsumerWarps];
   float s[kConsumerWarps];
   int g[kConsumerWarps];
-  int last;
-  int stop;  // uniform copy of the abort flag, written before a barrier
+  int stop;  // snapshot of the abort flag, taken before the barrier
 };
 
 template <int DT>
@@ -299,48 +189,72 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;  // elements per 16-byte vector
   extern __shared__ __align__(128) unsigned char smem[];
+  const int B = p.B, Kmax = p.Kmax, NC = p.nchunks, R = p.rows_per_req;
   unsigned char* stages = smem;
-  uint16_t* info = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes);
+  int* row_start = reinterpret_cast<int*>(smem + kStages * kStageBytes);        // [B + 1]
+  uint16_t* info = reinterpret_cast<uint16_t*>(row_start + ((B + 4) & ~3));     // [B]
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ StatsRed red[2];
-  __shared__ CombineSmem cs;
+  __shared__ int warp_tot[kStatsThreads / 32 + 1];
   __shared__ volatile int abort_flag;
-  __shared__ float xval_s;
 
   const int tid = threadIdx.x;
-  const int B = p.B, Kmax = p.Kmax, NC = p.nchunks, R = p.rows_per_req;
+  const int lane = tid & 31, warp = tid >> 5;
 
-  // prologue: request table + barriers
-  for (int i = tid; i < B; i += blockDim.x) {
-    uint32_t bad;
-    info[i] = request_info(p, i, &bad);
-    if (bad && blockIdx.x == 0) atomicOr(p.status, bad);
-  }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
+  // ---- prologue: per-request info and the row prefix (every CTA computes the same table) ----
+  {
+    const int per = (B + kStatsThreads - 1) / kStatsThreads;
+    const int lo = min(B, tid * per), hi = min(B, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) {
+      uint32_t bad;
+      info[i] = request_info(p, i, &bad);
+      if (bad && blockIdx.x == 0) atomicOr(p.status, bad);
+      local += rows_of(info[i]);
     }
-    abort_flag = 0;
-    fence_proxy_async_smem();
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    if (tid == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full_bar[s], 1);
+        mbar_init(&empty_bar[s], kConsumerWarps);
+      }
+      abort_flag = 0;
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int i = lo; i < hi; ++i) {
+      row_start[i] = run;
+      run += rows_of(info[i]);
+    }
+    if (tid == kStatsThreads - 1) row_start[B] = base + incl;
+    __syncthreads();
   }
-  __syncthreads();
-
-  const int64_t per_req = static_cast<int64_t>(R) * NC;
-  const int64_t total = per_req * B;
+  const int64_t T = static_cast<int64_t>(row_start[B]) * NC;
+  const int64_t t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
+  if (t0 >= t1) {
+    pdl_trigger();
+    return;
+  }
 
   if (tid >= kConsumerThreads) {
     // ---------------- producer warp: one lane issues the bulk copies ----------------
     if (tid == kConsumerThreads) {
-      const uint64_t pol = policy_evict_first();
+      int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
+      RowRef rr;
+      locate_row(row_start, info, Kmax, row, i, rr);
+      const char* src = row_base<DT>(p, rr);
       uint32_t it = 0;
-      for (int64_t s = blockIdx.x; s < total; s += gridDim.x) {
-        const int i = static_cast<int>(s / per_req);
-        const int rem = static_cast<int>(s - static_cast<int64_t>(i) * per_req);
-        const int r = rem / NC, c = rem - (rem / NC) * NC;
-        const int kind = slot_kind(info[i], r, c, Kmax);
-        if (kind == kSkip) continue;
+      for (int64_t t = t0; t < t1; ++t) {
         if (abort_flag) break;
         const int stage = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
@@ -349,21 +263,20 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
           abort_flag = 1;
           break;
         }
-        if (kind == kDummy) {
-          mbar_arrive(&full_bar[stage]);
-          continue;
-        }
-        const int64_t row = r <= Kmax ? target_row(p, i, r) : draft_row(p, i, r - Kmax - 1);
-        const char* src = r <= Kmax ? row_ptr<DT>(p.target, row, p.t_row_stride)
-                                    : row_ptr<DT>(p.draft, row, p.d_row_stride);
         const int c0 = c * p.chunk_len;
         const ChunkSplit sp = split_chunk<kElt>(src, c0, min(p.chunk_len, p.V - c0));
         if (sp.nvec == 0) {
           mbar_arrive(&full_bar[stage]);
         } else {
           mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(sp.nvec) * 16u);
+          // default L2 policy: the finalize kernel re-reads the rejected rows, often from L2
           bulk_g2s(stages + stage * kStageBytes, src + static_cast<int64_t>(c0 + sp.head) * kElt,
-                   static_cast<uint32_t>(sp.nvec) * 16u, &full_bar[stage], pol);
+                   static_cast<uint32_t>(sp.nvec) * 16u, &full_bar[stage]);
+        }
+        if (++c == NC && t + 1 < t1) {
+          c = 0;
+          locate_row(row_start, info, Kmax, ++row, i, rr);
+          src = row_base<DT>(p, rr);
         }
       }
       // drain: every issued copy must land before the CTA may exit
@@ -378,53 +291,57 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   }
 
   // ---------------- consumer warps ----------------
-  const int lane = tid & 31, warp = tid >> 5;
+  int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
+  RowRef rr;
+  locate_row(row_start, info, Kmax, row, i, rr);
   uint32_t it = 0;
   int buf = 0;
-  for (int64_t s = blockIdx.x; s < total; s += gridDim.x) {
-    const int i = static_cast<int>(s / per_req);
-    const int rem = static_cast<int>(s - static_cast<int64_t>(i) * per_req);
-    const int r = rem / NC, c = rem - (rem / NC) * NC;
-    const uint16_t inf = info[i];
-    const int kind = slot_kind(inf, r, c, Kmax);
-    if (kind == kSkip) continue;
+  bool row_open = false;
+  // per-row state
+  const char* rowp = nullptr;
+  bool sampled = false;
+  float kscale = 0.0f, m = -INFINITY, sacc = 0.0f, xfirst = NAN;
+  int g = -1, tok = -1, c_first = 0;
+  for (int64_t t = t0; t < t1; ++t) {
+    if (!row_open) {
+      const uint16_t inf = info[rr.i];
+      sampled = inf & kInfoSampled;
+      kscale = sampled ? kscale_of(__ldg(p.temperature + rr.i)) : 0.0f;
+      tok = (tid == 0 && sampled && rr.k < (inf & kInfoN))
+                ? __ldg(p.tokens + static_cast<int64_t>(rr.i) * p.tok_stride + rr.k) : -1;
+      rowp = row_base<DT>(p, rr);
+      c_first = c;
+      m = -INFINITY;
+      sacc = 0.0f;
+      g = -1;
+      xfirst = NAN;
+      row_open = true;
+    }
     const int stage = it % kStages;
     const uint32_t ph = (it / kStages) & 1u;
     ++it;
-
-    const bool sampled = inf & kInfoSampled;
-    const int n = inf & kInfoN;
-    const int k_row = r <= Kmax ? r : r - Kmax - 1;
-    float kscale = 0.0f;
-    if (sampled) kscale = kscale_of(__ldg(p.temperature + i));
-    int tok = -1;
-    if (tid == 0 && kind == kLoad && sampled && k_row < n)
-      tok = __ldg(p.tokens + static_cast<int64_t>(i) * p.tok_stride + k_row);
-
     const int c0 = c * p.chunk_len;
-    const int len = kind == kLoad ? min(p.chunk_len, p.V - c0) : 0;
-    const char* rowp = nullptr;
-    if (kind == kLoad) {
-      const int64_t row = r <= Kmax ? target_row(p, i, r) : draft_row(p, i, r - Kmax - 1);
-      rowp = r <= Kmax ? row_ptr<DT>(p.target, row, p.t_row_stride) : row_ptr<DT>(p.draft, row, p.d_row_stride);
-    }
-    const ChunkSplit sp = kind == kLoad ? split_chunk<kElt>(rowp, c0, len) : ChunkSplit{0, 0, 0};
+    const int len = min(p.chunk_len, p.V - c0);
+    const ChunkSplit sp = split_chunk<kElt>(rowp, c0, len);
     const int head = sp.head, nvec = sp.nvec, tail = sp.tail;
-    const int v0 = c0 + head;                      // vocabulary index of the first staged element
-    const int t0 = v0 + nvec * kVec;               // first tail element
+    const int v0 = c0 + head;         // vocabulary index of the first staged element
+    const int te = v0 + nvec * kVec;  // first tail element
 
-    // A timed-out wait does not leave the loop here: every consumer thread must reach the same
-    // named barriers; the abort decision is taken uniformly after them.
-    if (!mbar_wait(&full_bar[stage], ph, p.status)) abort_flag = 1;
+    // Warp 0 waits for the stage (backed-off polling); the other warps sleep in the named
+    // barrier, which orders their shared-memory reads after the completed bulk copy.  After a
+    // timeout the remaining tasks run on whatever the stage holds; the loop leaves at the next
+    // row end, where every consumer thread reads the same abort snapshot.
+    if (warp == 0 && !abort_flag && !mbar_wait(&full_bar[stage], ph, p.status)) abort_flag = 1;
+    named_bar(2, kConsumerThreads);
     const unsigned char* sb = stages + stage * kStageBytes;
     uint4 raw[kVecPerThread];
 #pragma unroll
     for (int j = 0; j < kVecPerThread; ++j) {
       const int v = tid + j * kConsumerThreads;
-      raw[j] = v < nvec ? lds128(sb + v * 16) : make_uint4(0, 0, 0, 0);
+      raw[j] = v < nvec ? lds128(sb + v * 16) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
     }
     float xval = NAN;
-    if (tid == 0 && tok >= v0 && tok < t0) {
+    if (tid == 0 && tok >= v0 && tok < te) {
       if constexpr (DT == SV_BF16)
         xval = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[tok - v0]) << 16);
       else
@@ -435,15 +352,16 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 
     // head / tail elements outside the 16-byte aligned interior: plain loads
     const bool has_head = tid < head, has_tail = tid < tail;
-    const float head_x = has_head ? load_logit<DT>(rowp, c0 + tid) : 0.0f;
-    const float tail_x = has_tail ? load_logit<DT>(rowp, t0 + tid) : 0.0f;
-    if (tid == 0 && kind == kLoad && tok >= c0 && tok < c0 + len && !(tok >= v0 && tok < t0))
-      xval = load_logit<DT>(rowp, tok);
+    const float head_x = has_head ? load_logit<DT>(rowp, c0 + tid) : -INFINITY;
+    const float tail_x = has_tail ? load_logit<DT>(rowp, te + tid) : -INFINITY;
+    if (tid == 0 && tok >= c0 && tok < c0 + len && !(tok >= v0 && tok < te)) xval = load_logit<DT>(rowp, tok);
 
-    float m = -INFINITY, sacc = 0.0f;
-    int g = -1;
     if (!sampled) {
-      if (has_head) { m = head_x; g = c0 + tid; }
+      // running first argmax (elements visited in increasing vocabulary order)
+      if (has_head && (g < 0 || head_x > m)) {
+        m = head_x;
+        g = c0 + tid;
+      }
 #pragma unroll
       for (int j = 0; j < kVecPerThread; ++j) {
         const int v = tid + j * kConsumerThreads;
@@ -454,42 +372,54 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
-              if (g < 0 || lo > m) { m = lo; g = base + 2 * e; }
-              if (hi > m) { m = hi; g = base + 2 * e + 1; }
+              if (g < 0 || lo > m) {
+                m = lo;
+                g = base + 2 * e;
+              }
+              if (hi > m) {
+                m = hi;
+                g = base + 2 * e + 1;
+              }
             }
           } else {
             const float w[4] = {__uint_as_float(raw[j].x), __uint_as_float(raw[j].y),
                                 __uint_as_float(raw[j].z), __uint_as_float(raw[j].w)};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (g < 0 || w[e] > m) { m = w[e]; g = base + e; }
+              if (g < 0 || w[e] > m) {
+                m = w[e];
+                g = base + e;
+              }
           }
         }
       }
-      if (has_tail && (g < 0 || tail_x > m)) { m = tail_x; g = t0 + tid; }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-        const int g2 = __shfl_xor_sync(0xFFFFFFFFu, g, o);
-        merge_argmax(m, g, m2, g2);
+      if (has_tail && (g < 0 || tail_x > m)) {
+        m = tail_x;
+        g = te + tid;
       }
     } else {
+      // chunk max (packed bf16x2 max where possible), then rescale the running sum once
+      float mc;
+      if constexpr (DT == SV_BF16) {
+        uint32_t w = bf16x2_max(bf16x2_max(raw[0].x, raw[0].y), bf16x2_max(raw[0].z, raw[0].w));
 #pragma unroll
-      for (int j = 0; j < kVecPerThread; ++j) {
-        if (tid + j * kConsumerThreads < nvec) {
-          if constexpr (DT == SV_BF16) {
-            m = fmaxf(m, fmaxf(fmaxf(bf16_lo(raw[j].x), bf16_hi(raw[j].x)), fmaxf(bf16_lo(raw[j].y), bf16_hi(raw[j].y))));
-            m = fmaxf(m, fmaxf(fmaxf(bf16_lo(raw[j].z), bf16_hi(raw[j].z)), fmaxf(bf16_lo(raw[j].w), bf16_hi(raw[j].w))));
-          } else {
-            m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(raw[j].x), __uint_as_float(raw[j].y)),
+        for (int j = 1; j < kVecPerThread; ++j)
+          w = bf16x2_max(w, bf16x2_max(bf16x2_max(raw[j].x, raw[j].y), bf16x2_max(raw[j].z, raw[j].w)));
+        mc = fmaxf(bf16_lo(w), bf16_hi(w));
+      } else {
+        mc = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kVecPerThread; ++j)
+          mc = fmaxf(mc, fmaxf(fmaxf(__uint_as_float(raw[j].x), __uint_as_float(raw[j].y)),
                                fmaxf(__uint_as_float(raw[j].z), __uint_as_float(raw[j].w))));
-          }
-        }
       }
-      if (has_head) m = fmaxf(m, head_x);
-      if (has_tail) m = fmaxf(m, tail_x);
+      mc = fmaxf(mc, fmaxf(head_x, tail_x));
+      if (mc > m) {
+        sacc = (m == -INFINITY) ? 0.0f : sacc * ex2_approx((m - mc) * kscale);
+        m = mc;
+      }
       if (m != -INFINITY) {
-        if (has_head) sacc += ex2_approx((head_x - m) * kscale);
+        float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < kVecPerThread; ++j) {
           if (tid + j * kConsumerThreads < nvec) {
@@ -497,289 +427,669 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
               const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                sacc += ex2_approx((bf16_lo(w[e]) - m) * kscale);
-                sacc += ex2_approx((bf16_hi(w[e]) - m) * kscale);
+                acc += ex2_approx((bf16_lo(w[e]) - m) * kscale);
+                acc += ex2_approx((bf16_hi(w[e]) - m) * kscale);
               }
             } else {
-              sacc += ex2_approx((__uint_as_float(raw[j].x) - m) * kscale);
-              sacc += ex2_approx((__uint_as_float(raw[j].y) - m) * kscale);
-              sacc += ex2_approx((__uint_as_float(raw[j].z) - m) * kscale);
-              sacc += ex2_approx((__uint_as_float(raw[j].w) - m) * kscale);
+              acc += ex2_approx((__uint_as_float(raw[j].x) - m) * kscale);
+              acc += ex2_approx((__uint_as_float(raw[j].y) - m) * kscale);
+              acc += ex2_approx((__uint_as_float(raw[j].z) - m) * kscale);
+              acc += ex2_approx((__uint_as_float(raw[j].w) - m) * kscale);
             }
           }
         }
-        if (has_tail) sacc += ex2_approx((tail_x - m) * kscale);
+        if (has_head) acc += ex2_approx((head_x - m) * kscale);
+        if (has_tail) acc += ex2_approx((tail_x - m) * kscale);
+        sacc += acc;
       }
+    }
+
+    ChunkRecord* rec_row = p.rec + (static_cast<int64_t>(rr.i) * R + rr.rec_row) * NC;
+    if (tid == 0) {
+      if (c == c_first) {
+        xfirst = xval;
+      } else {
+        // empty record: this chunk's statistics live in the piece's first record
+        __stcg(reinterpret_cast<float4*>(rec_row + c), make_float4(-INFINITY, 0.0f, __int_as_float(-1), xval));
+      }
+    }
+
+    const bool row_end = (c == NC - 1) || (t + 1 == t1);
+    if (row_end) {
+      // reduce the piece across threads and write its record
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sacc, o);
-        merge_ms(m, sacc, m2, s2, kscale);
-      }
-    }
-    if (lane == 0) {
-      red[buf].m[warp] = m;
-      red[buf].s[warp] = sacc;
-      red[buf].g[warp] = g;
-    }
-    if (tid == 0) xval_s = xval;
-    named_bar(1, kConsumerThreads);
-    if (warp == 0) {
-      float mm = lane < kConsumerWarps ? red[buf].m[lane] : -INFINITY;
-      float ss = lane < kConsumerWarps ? red[buf].s[lane] : 0.0f;
-      int gg = lane < kConsumerWarps ? red[buf].g[lane] : -1;
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mm, o);
-        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-        const int g2 = __shfl_xor_sync(0xFFFFFFFFu, gg, o);
-        if (sampled) merge_ms(mm, ss, m2, s2, kscale);
-        else merge_argmax(mm, gg, m2, g2);
+        if (sampled) {
+          const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sacc, o);
+          merge_ms(m, sacc, m2, s2, kscale);
+        } else {
+          const int g2 = __shfl_xor_sync(0xFFFFFFFFu, g, o);
+          merge_argmax(m, g, m2, g2);
+        }
       }
       if (lane == 0) {
-        if (kind == kLoad) {
-          float4 rec;
-          rec.x = mm;
-          rec.y = sampled ? ss : 0.0f;
-          rec.z = __int_as_float(sampled ? -1 : gg);
-          rec.w = xval_s;
-          __stcg(reinterpret_cast<float4*>(p.rec + (static_cast<int64_t>(i) * R + r) * NC + c), rec);
-        }
-        __threadfence();
-        const uint32_t old = atomicAdd(p.cnt_stats + i, 1u);
-        red[buf].last = (old + 1u == expected_tasks(inf, NC)) ? 1 : 0;
-        red[buf].stop = abort_flag;
-        __threadfence();
+        red[buf].m[warp] = m;
+        red[buf].s[warp] = sacc;
+        red[buf].g[warp] = g;
       }
+      if (tid == 0) red[buf].stop = abort_flag;
+      // red[] is double-buffered: a warp writes red[buf] again two row ends later, after the
+      // next barrier, by which time warp 0 has read it.
+      named_bar(1, kConsumerThreads);
+      if (warp == 0) {
+        float mm = lane < kConsumerWarps ? red[buf].m[lane] : -INFINITY;
+        float ss = lane < kConsumerWarps ? red[buf].s[lane] : 0.0f;
+        int gg = lane < kConsumerWarps ? red[buf].g[lane] : -1;
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mm, o);
+          const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+          const int g2 = __shfl_xor_sync(0xFFFFFFFFu, gg, o);
+          if (sampled) merge_ms(mm, ss, m2, s2, kscale);
+          else merge_argmax(mm, gg, m2, g2);
+        }
+        if (lane == 0)
+          __stcg(reinterpret_cast<float4*>(rec_row + c_first),
+                 make_float4(mm, sampled ? ss : 0.0f, __int_as_float(sampled ? -1 : gg), xfirst));
+      }
+      const int stop = red[buf].stop;
+      buf ^= 1;
+      row_open = false;
+      if (stop) break;
     }
-    named_bar(1, kConsumerThreads);
-    if (red[buf].last) combine_request(p, i, inf, tid, &cs);
-    if (red[buf].stop) break;
-    buf ^= 1;
+    if (++c == NC && t + 1 < t1) {
+      c = 0;
+      locate_row(row_start, info, Kmax, ++row, i, rr);
+    }
   }
   pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------------
-// sample kernel: grid (nchunks, B)
+// finalize kernel: grid (nchunks, B) for sampled calls, (1, B) for greedy calls
 // ------------------------------------------------------------------------------------------
-struct SampleSmem {
-  ReqState st;
-  float wsum[kSampleThreads / 32];
-  float seg_excl[kSampleThreads];
-  int pick_thread;
-  int last_pos;
-  int last;
-  int chunk;
-  double base;
-  double Z;
-  int use_bonus_row;
-  uint32_t flags;
+// Per-row statistics in shared memory (one entry per record row of the request).
+struct RowStatS {
+  float s;     // sum of 2^((x - m) k) over the row (merged over chunks in double)
+  float m;     // row max
+  int32_t g;   // first argmax (greedy rows)
+  float xval;  // logit at the row's drafted token (sampled rows)
 };
 
-// weight of vocabulary entry v (index inside the chunk) for the draw
+constexpr size_t kFinMaxStagedBytes = 48 * 1024;
+constexpr int kMaxRange = 1024;  // longest warp range: a 16 KB chunk of bf16 split eight ways  // records staged in shared memory up to this size
+constexpr int kFinMaxDynSmem = 96 * 1024;
+
+struct FinSmem {
+  ReqState st;      // what the draw needs (identical in every CTA of the request)
+  int a_min;
+  uint32_t acc_flags;
+  uint32_t bad;
+  float wsum[kSampleWarps];
+  int last;
+  int chunk;        // crossing chunk
+  int bonus;        // draw from the target row (bonus, or residual mass 0)
+  uint32_t flags;
+  float base;       // mass before the crossing chunk
+  float thr;        // u' * Z
+  float wbuf[kMaxRange + kMaxRange / 32];  // draw weights of the crossing warp range (skewed)
+};
+
+// weight of vocabulary entry v of a row pair for the draw (target-only when !residual)
 template <int DT>
-__device__ __forceinline__ float draw_weight(const unsigned char* tb, const unsigned char* db, int v, bool residual,
+__device__ __forceinline__ float draw_weight(const char* trow, const char* drow, int64_t v, bool residual,
                                              const ReqState& st) {
-  float t, d = 0.0f;
-  if constexpr (DT == SV_BF16) {
-    t = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(tb)[v]) << 16);
-    if (residual) d = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(db)[v]) << 16);
-  } else {
-    t = reinterpret_cast<const float*>(tb)[v];
-    if (residual) d = reinterpret_cast<const float*>(db)[v];
-  }
-  const float pv = ex2_approx((t - st.mt) * st.kscale);
+  const float pv = ex2_approx((load_logit<DT>(trow, v) - st.mt) * st.kscale);
   if (!residual) return pv;
-  return fmaxf(0.0f, pv * st.inv_st - ex2_approx((d - st.md) * st.kscale) * st.inv_sd);
+  return fmaxf(0.0f, pv * st.inv_st - ex2_approx((load_logit<DT>(drow, v) - st.md) * st.kscale) * st.inv_sd);
 }
 
-// Copy `len` elements of a row chunk into shared memory (16-byte vectors + scalar tail).
+// The eight warp ranges of a chunk: contiguous, warp w covers [lo, hi).
+__device__ __forceinline__ void warp_range(int len, int w, int* lo, int* hi) {
+  const int seg = (len + kSampleWarps - 1) / kSampleWarps;
+  *lo = min(len, w * seg);
+  *hi = min(len, *lo + seg);
+}
+
+// Sum of draw weights over [c0 + lo, c0 + hi) by one warp.  A warp range holds at most 128
+// 16-byte vectors, so each lane issues all of its loads (<= 4 per row) before using any.
+constexpr int kRangeVecPerLane = 4;
 template <int DT>
-__device__ void stage_chunk(unsigned char* dst, const char* src, int len, int tid) {
+__device__ float warp_range_sum(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
+                                const ReqState& st, int lane) {
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
-  const int nvec = (reinterpret_cast<uintptr_t>(src) & 15u) ? 0 : ((len * kElt) >> 4);
-  for (int v = tid; v < nvec; v += kSampleThreads)
-    reinterpret_cast<uint4*>(dst)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
-  for (int e = nvec * (16 / kElt) + tid; e < len; e += kSampleThreads) {
-    if constexpr (DT == SV_BF16)
-      reinterpret_cast<uint16_t*>(dst)[e] = __ldg(reinterpret_cast<const uint16_t*>(src) + e);
-    else
-      reinterpret_cast<float*>(dst)[e] = __ldg(reinterpret_cast<const float*>(src) + e);
+  constexpr int kVec = 16 / kElt;
+  float acc = 0.0f;
+  const int len = hi - lo;
+  const ChunkSplit a = split_chunk<kElt>(trow, c0 + lo, len);
+  const ChunkSplit b = residual ? split_chunk<kElt>(drow, c0 + lo, len) : a;
+  if (a.nvec > 0 && a.head == b.head && a.nvec <= 32 * kRangeVecPerLane) {
+    const int v0 = c0 + lo + a.head;
+    const uint4* tv = reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(v0) * kElt);
+    const uint4* dv = reinterpret_cast<const uint4*>(drow + static_cast<int64_t>(v0) * kElt);
+    uint4 tw[kRangeVecPerLane], dw[kRangeVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kRangeVecPerLane; ++u) {
+      const int v = lane + 32 * u;
+      tw[u] = v < a.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
+      dw[u] = (residual && v < a.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
+    }
+    const float hx = lane < a.head ? draw_weight<DT>(trow, drow, c0 + lo + lane, residual, st) : 0.0f;
+    const float tx_ = lane < a.tail ? draw_weight<DT>(trow, drow, v0 + a.nvec * kVec + lane, residual, st) : 0.0f;
+#pragma unroll
+    for (int u = 0; u < kRangeVecPerLane; ++u) {
+      if (lane + 32 * u >= a.nvec) break;
+      float tx[kVec], dx[kVec];
+      if constexpr (DT == SV_BF16) {
+        const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          tx[2 * e] = bf16_lo(t4[e]);
+          tx[2 * e + 1] = bf16_hi(t4[e]);
+          dx[2 * e] = bf16_lo(d4[e]);
+          dx[2 * e + 1] = bf16_hi(d4[e]);
+        }
+      } else {
+        tx[0] = __uint_as_float(tw[u].x);
+        tx[1] = __uint_as_float(tw[u].y);
+        tx[2] = __uint_as_float(tw[u].z);
+        tx[3] = __uint_as_float(tw[u].w);
+        dx[0] = __uint_as_float(dw[u].x);
+        dx[1] = __uint_as_float(dw[u].y);
+        dx[2] = __uint_as_float(dw[u].z);
+        dx[3] = __uint_as_float(dw[u].w);
+      }
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
+        acc += residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
+      }
+    }
+    acc += hx + tx_;
+  } else {
+#pragma unroll 8
+    for (int e = lane; e < len; e += 32) acc += draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
 }
 
-// Inverse-CDF pick inside one staged chunk: first v with base + cumsum_{w<=v} > thr.
+// Inverse-CDF pick inside [lo, hi) of a chunk (hi - lo <= kMaxRange) by one warp.  The range's
+// weights are computed once (all loads issued together) into shared memory, skewed by one slot
+// per 32 so that each lane can walk its own contiguous 32 entries without bank conflicts.
+// Returns the first v with base + cumsum > thr, or, if rounding keeps every partial sum at or
+// below thr, the last entry with positive weight (-1 if none).
 template <int DT>
-__device__ int scan_pick(const unsigned char* tb, const unsigned char* db, int len, bool residual,
-                         const ReqState& st, double base, double thr, int tid, SampleSmem* sm) {
-  const int seg = (len + kSampleThreads - 1) / kSampleThreads;
-  const int lo = min(len, tid * seg), hi = min(len, lo + seg);
+__device__ int warp_pick(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
+                         const ReqState& st, float base, float thr, int lane, float* wbuf) {
+  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
+  constexpr int kVec = 16 / kElt;
+  const int len = hi - lo;
+  const ChunkSplit sa = split_chunk<kElt>(trow, c0 + lo, len);
+  const ChunkSplit sb = residual ? split_chunk<kElt>(drow, c0 + lo, len) : sa;
+  if (sa.nvec > 0 && sa.head == sb.head && sa.nvec <= 32 * kRangeVecPerLane) {
+    // 16-byte vectors, every load issued before any is used
+    const int v0 = lo + sa.head;  // chunk-relative index of the first vector element
+    const uint4* tv = reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(c0 + v0) * kElt);
+    const uint4* dv = reinterpret_cast<const uint4*>(drow + static_cast<int64_t>(c0 + v0) * kElt);
+    uint4 tw[kRangeVecPerLane], dw[kRangeVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kRangeVecPerLane; ++u) {
+      const int v = lane + 32 * u;
+      tw[u] = v < sa.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
+      dw[u] = (residual && v < sa.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
+    }
+    if (lane < sa.head) {
+      const int e = lane;
+      wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+    }
+    if (lane < sa.tail) {
+      const int e = sa.head + sa.nvec * kVec + lane;
+      wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+    }
+#pragma unroll
+    for (int u = 0; u < kRangeVecPerLane; ++u) {
+      const int v = lane + 32 * u;
+      if (v >= sa.nvec) break;
+      float tx[kVec], dx[kVec];
+      if constexpr (DT == SV_BF16) {
+        const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          tx[2 * e] = bf16_lo(t4[e]);
+          tx[2 * e + 1] = bf16_hi(t4[e]);
+          dx[2 * e] = bf16_lo(d4[e]);
+          dx[2 * e + 1] = bf16_hi(d4[e]);
+        }
+      } else {
+        tx[0] = __uint_as_float(tw[u].x);
+        tx[1] = __uint_as_float(tw[u].y);
+        tx[2] = __uint_as_float(tw[u].z);
+        tx[3] = __uint_as_float(tw[u].w);
+        dx[0] = __uint_as_float(dw[u].x);
+        dx[1] = __uint_as_float(dw[u].y);
+        dx[2] = __uint_as_float(dw[u].z);
+        dx[3] = __uint_as_float(dw[u].w);
+      }
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
+        const float w =
+            residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
+        const int idx = sa.head + v * kVec + e;  // range-relative element
+        wbuf[idx + (idx >> 5)] = w;
+      }
+    }
+  } else {
+#pragma unroll 8
+    for (int e = lane; e < len; e += 32) wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+  }
+  __syncwarp();
+  const int a = min(len, lane * 32), b = min(len, a + 32);
   float ssum = 0.0f;
   int lastpos = -1;
-  for (int v = lo; v < hi; ++v) {
-    const float w = draw_weight<DT>(tb, db, v, residual, st);
+  for (int e = a; e < b; ++e) {
+    const float w = wbuf[e + (e >> 5)];
     ssum += w;
-    if (w > 0.0f) lastpos = v;
+    if (w > 0.0f) lastpos = e;
   }
-  // block exclusive scan of segment sums (sequential over warps' totals; deterministic)
-  const int lane = tid & 31, warp = tid >> 5;
   float incl = ssum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += y;
   }
-  if (lane == 31) sm->wsum[warp] = incl;
-  if (tid == 0) {
-    sm->pick_thread = kSampleThreads;
-    sm->last_pos = -1;
-  }
-  __syncthreads();
-  float wbase = 0.0f;
-  for (int w = 0; w < warp; ++w) wbase += sm->wsum[w];
-  const float excl = wbase + incl - ssum;
-  const float rem = static_cast<float>(thr - base);
-  if (hi > lo && ssum > 0.0f && excl + ssum > rem) atomicMin(&sm->pick_thread, tid);
-  if (lastpos >= 0) atomicMax(&sm->last_pos, lastpos);
-  __syncthreads();
+  const float excl = incl - ssum;
+  const float rem = thr - base;
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, b > a && ssum > 0.0f && excl + ssum > rem);
   int y = -1;
-  if (tid == sm->pick_thread) {
-    float run = excl;
-    for (int v = lo; v < hi; ++v) {
-      const float w = draw_weight<DT>(tb, db, v, residual, st);
-      run += w;
-      if (run > rem && w > 0.0f) {
-        y = v;
-        break;
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    if (lane == src) {
+      float run = excl;
+      for (int e = a; e < b; ++e) {
+        const float w = wbuf[e + (e >> 5)];
+        run += w;
+        if (w > 0.0f && run > rem) {
+          y = e;
+          break;
+        }
       }
+      if (y < 0) y = lastpos;
     }
-    if (y < 0) y = lastpos;  // rounding: stay on the last positive weight of this segment
-    sm->last_pos = y;
+    y = __shfl_sync(0xFFFFFFFFu, y, src);
+  } else {
+    int lp = lastpos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
+    y = lp;
   }
-  __syncthreads();
-  return sm->last_pos;  // pick (or the last positive entry of the chunk if no segment crossed)
+  return y < 0 ? -1 : lo + y;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kSampleThreads) sample_kernel(const VerifyParams p) {
-  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
-  __shared__ __align__(16) unsigned char tbuf[kStageBytes];
-  __shared__ __align__(16) unsigned char dbuf[kStageBytes];
-  __shared__ SampleSmem sm;
-  pdl_wait();
-  const int tid = threadIdx.x;
-  const int i = blockIdx.y, c = blockIdx.x;
-  const int NC = p.nchunks;
-  if (tid == 0) sm.st = p.req[i];
-  __syncthreads();
-  const ReqState& st = sm.st;
-  if (st.mode == kModeNone) return;
-  if (st.mode == kModeBonus && c != 0) return;
-
-  bool residual = st.mode == kModeResidual;
-  if (residual) {
-    // chunk residual mass
-    const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
-    const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride) + static_cast<int64_t>(c0) * kElt;
-    const char* drow = row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) + static_cast<int64_t>(c0) * kElt;
-    stage_chunk<DT>(tbuf, trow, len, tid);
-    stage_chunk<DT>(dbuf, drow, len, tid);
-    __syncthreads();
-    float acc = 0.0f;
-    for (int v = tid; v < len; v += kSampleThreads) acc += draw_weight<DT>(tbuf, dbuf, v, true, st);
+// First index j in [0, cnt) whose running sum of w(j) (float, index order) exceeds thr, found by
+// one warp.  Returns j (or the last j with w > 0 when rounding keeps every sum <= thr) and the sum
+// of the entries before it in *before.
+template <typename WF>
+__device__ int warp_find(int cnt, float thr, WF w, float* before, int lane) {
+  float run = 0.0f;
+  int last_pos = -1;
+  float before_last = 0.0f;
+  for (int j0 = 0; j0 < cnt; j0 += 32) {
+    const int j = j0 + lane;
+    const float wj = j < cnt ? w(j) : 0.0f;
+    float incl = wj;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if ((tid & 31) == 0) sm.wsum[tid >> 5] = acc;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < cnt && wj > 0.0f && run + incl > thr);
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < cnt && wj > 0.0f);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      *before = run + __shfl_sync(0xFFFFFFFFu, incl - wj, src);
+      return j0 + src;
+    }
+    if (pos) {
+      const int src = 31 - __clz(pos);
+      last_pos = j0 + src;
+      before_last = run + __shfl_sync(0xFFFFFFFFu, incl - wj, src);
+    }
+    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  *before = last_pos >= 0 ? before_last : 0.0f;
+  return last_pos >= 0 ? last_pos : 0;
+}
+
+// Shared-memory plan of the finalize kernel: row statistics, then (when they fit) the request's
+// staged chunk records, then its drafted tokens.
+struct FinLayout {
+  size_t rec_off, tok_off, bytes;
+  bool staged;
+};
+__host__ __device__ inline FinLayout fin_layout(int R, int NC, int Kmax) {
+  FinLayout L;
+  const size_t rows = static_cast<size_t>(R) * sizeof(RowStatS);
+  const size_t recs = static_cast<size_t>(R) * NC * sizeof(ChunkRecord);
+  L.staged = recs <= kFinMaxStagedBytes;
+  L.rec_off = rows;
+  L.tok_off = rows + (L.staged ? recs : 0);
+  L.bytes = L.tok_off + ((static_cast<size_t>(Kmax) * 4 + 15) & ~size_t(15));
+  return L;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int DT>
+__global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyParams p) {
+  extern __shared__ __align__(16) unsigned char fin_dyn[];
+  __shared__ FinSmem sm;
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.y, c = blockIdx.x;
+  const int NC = p.nchunks, R = p.rows_per_req, Kmax = p.Kmax;
+  const FinLayout FL = fin_layout(R, NC, Kmax);
+  RowStatS* rs = reinterpret_cast<RowStatS*>(fin_dyn);                        // [R]
+  ChunkRecord* rec_s = reinterpret_cast<ChunkRecord*>(fin_dyn + FL.rec_off);  // [R * NC] if staged
+  int32_t* tok_s = reinterpret_cast<int32_t*>(fin_dyn + FL.tok_off);          // [Kmax]
+  const ChunkRecord* rec_g = p.rec + static_cast<int64_t>(i) * R * NC;
+  const int32_t* toks = p.tokens ? p.tokens + static_cast<int64_t>(i) * p.tok_stride : nullptr;
+
+  // ---------------- round 1: everything the combine reads, requested at once ----------------
+  // (records of all 2*Kmax+1 record rows and all Kmax tokens; entries past n are ignored)
+  if (FL.staged)
+    for (int j = tid; j < R * NC; j += kSampleThreads) cp_async16(rec_s + j, rec_g + j);
+  if (toks)
+    for (int j = tid; j < Kmax; j += kSampleThreads) cp_async4(tok_s + j, toks + j);
+  uint32_t bad_in;
+  const uint16_t info = request_info(p, i, &bad_in);  // row_stats' CTA 0 reported bad_in already
+  const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
+  const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
+  cp_async_wait_all();
+  __syncthreads();
+  if (info & kInfoInvalid) {
+    if (c == 0) write_invalid(p, i, tid, kSampleThreads);
+    return;
+  }
+  const int n = info & kInfoN;
+  const bool sampled = info & kInfoSampled;
+  if (!sampled && c > 0) return;
+  const bool need_draft = info & kInfoNeedDraft;
+  const float kscale = sampled ? kscale_of(T) : 0.0f;
+  const int nrows = n + 1 + (need_draft ? n : 0);
+  const ChunkRecord* recs = FL.staged ? rec_s : rec_g;
+  auto tok = [&](int k) { return toks ? tok_s[k] : rs[Kmax + 1 + k].g; };
+
+  // 1. row statistics: one warp per row, one pass over the row's chunk records
+  for (int q = warp; q < nrows; q += kSampleWarps) {
+    const bool is_target = q <= n;
+    const int k = is_target ? q : q - n - 1;
+    const int r = is_target ? k : Kmax + 1 + k;
+    const ChunkRecord* rr = recs + static_cast<int64_t>(r) * NC;
+    const int x = (sampled && k < n) ? tok_s[k] : -1;  // drafted token of this row
+    const int cx = (x >= 0 && x < p.V) ? x / p.chunk_len : -1;
+    float m = -INFINITY, xval = NAN, S = 0.0f;
+    int g = -1;
+    if (sampled) {
+      // row max, then the chunk sums rescaled to it, added with a compensated (TwoSum) tree
+      for (int cc = lane; cc < NC; cc += 32) {
+        const ChunkRecord rc = FL.staged ? rr[cc] : ld_record(rr + cc);
+        m = fmaxf(m, rc.m);
+        if (cc == cx) xval = rc.xval;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      float hi = 0.0f, lo = 0.0f;
+      if (m != -INFINITY) {
+        for (int cc = lane; cc < NC; cc += 32) {
+          const ChunkRecord rc = FL.staged ? rr[cc] : ld_record(rr + cc);
+          if (rc.m != -INFINITY) two_sum_acc(hi, lo, rc.s * exp2f((rc.m - m) * kscale));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o), l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+        two_sum_acc(hi, lo, h2);
+        lo += l2;
+      }
+      S = hi + lo;
+    } else {
+      for (int cc = lane; cc < NC; cc += 32) {
+        const ChunkRecord rc = FL.staged ? rr[cc] : ld_record(rr + cc);
+        merge_argmax(m, g, rc.m, rc.g);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const int g2 = __shfl_xor_sync(0xFFFFFFFFu, g, o);
+        merge_argmax(m, g, m2, g2);
+      }
+    }
+    if (cx >= 0) xval = __shfl_sync(0xFFFFFFFFu, xval, cx & 31);
+    if (lane == 0) {
+      rs[r].s = S;
+      rs[r].m = m;
+      rs[r].g = g;
+      rs[r].xval = xval;
+    }
+  }
+  if (tid == 0) {
+    sm.a_min = n;
+    sm.acc_flags = 0;
+    sm.bad = 0;
+  }
+  __syncthreads();
+
+  // 2. accept tests (each position independently; the first rejection is a min-reduction)
+  for (int k = tid; k < n; k += kSampleThreads) {
+    const int x = tok(k);
+    bool acc;
+    float pv, qv;
+    if (x < 0 || x >= p.V) {
+      atomicOr(&sm.bad, SV_DEV_BAD_TOKEN);
+      acc = false;
+      pv = qv = NAN;
+    } else if (!sampled) {
+      acc = (x == rs[k].g);
+      pv = acc ? 1.0f : 0.0f;
+      qv = 1.0f;
+    } else {
+      const RowStatS rt = rs[k], rd = rs[Kmax + 1 + k];
+      pv = __fdiv_rn(exp2f((rt.xval - rt.m) * kscale), rt.s);
+      qv = __fdiv_rn(exp2f((rd.xval - rd.m) * kscale), rd.s);
+      const float u = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 0u, p.round);
+      acc = u * qv < pv;
+      if (qv == 0.0f) atomicOr(&sm.acc_flags, SV_FLAG_Q_ZERO);
+    }
+    if (c == 0 && p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = pv;
+    if (c == 0 && p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = qv;
+    if (!acc) atomicMin(&sm.a_min, k);
+  }
+  if (c == 0) {
+    for (int k = n + tid; k < Kmax; k += kSampleThreads) {
+      if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
+      if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
+    }
+  }
+  __syncthreads();
+  if (sm.bad) {
+    if (c == 0) {
+      if (tid == 0) atomicOr(p.status, sm.bad);
+      write_invalid(p, i, tid, kSampleThreads);
+    }
+    return;
+  }
+  const int a = sm.a_min;
+
+  // 3. emit: the accepted prefix (and, greedy, the target argmax at a); a sampled request's
+  //    token at a is written by the CTA that draws it
+  if (c == 0) {
+    for (int j = tid; j <= Kmax; j += kSampleThreads) {
+      if (j == a && sampled) continue;
+      int v = -1;
+      if (j < a) v = tok(j);
+      else if (j == a) v = rs[a].g;
+      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
+    }
+    if (tid == 0) {
+      p.out_accept_len[i] = a;
+      if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(sm.acc_flags);
+    }
+  }
+  if (!sampled) return;
+  const int mode = a < n ? kModeResidual : kModeBonus;
+  if (mode == kModeBonus && c != 0) return;
+  if (tid == 0) {
+    ReqState st = {};
+    st.mode = mode;
+    st.a = a;
+    st.flags = static_cast<int32_t>(sm.acc_flags);
+    st.row_t = target_row(p, i, a);
+    st.kscale = kscale;
+    st.mt = rs[a].m;
+    st.st = rs[a].s;
+    st.inv_st = __frcp_rn(rs[a].s);
+    if (mode == kModeResidual) {
+      st.row_d = draft_row(p, i, a);
+      st.md = rs[Kmax + 1 + a].m;
+      st.inv_sd = __frcp_rn(rs[Kmax + 1 + a].s);
+    }
+    st.rec_row_t = a;  // record row inside the request
+    st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
+    sm.st = st;
+  }
+  __syncthreads();
+
+  // ---------------- draw at position a ----------------
+  const ReqState& st = sm.st;
+  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
+  const char* drow = st.mode == kModeResidual ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
+  float* wm = p.wmass + static_cast<int64_t>(i) * NC * kSampleWarps;
+  float* mass_s = reinterpret_cast<float*>(fin_dyn + FL.rec_off);  // reuses the staged records' space
+  const bool stage_mass = FL.staged && static_cast<size_t>(NC) * (kSampleWarps + 1) * 4 <=
+                                           static_cast<size_t>(R) * NC * sizeof(ChunkRecord);
+
+  if (st.mode == kModeResidual) {
+    // this CTA's chunk: per-warp-range and per-chunk residual masses
+    const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+    int lo, hi;
+    warp_range(len, warp, &lo, &hi);
+    const float ws = warp_range_sum<DT>(trow, drow, c0, lo, hi, true, st, lane);
+    if (lane == 0) {
+      sm.wsum[warp] = ws;
+      __stcg(wm + c * kSampleWarps + warp, ws);
+    }
     __syncthreads();
     if (tid == 0) {
       float tot = 0.0f;
-      for (int w = 0; w < kSampleThreads / 32; ++w) tot += sm.wsum[w];
+      for (int w = 0; w < kSampleWarps; ++w) tot += sm.wsum[w];
       __stcg(p.mass + static_cast<int64_t>(i) * NC + c, tot);
-      __threadfence();
-      const uint32_t old = atomicAdd(p.cnt_sample + i, 1u);
+      const uint32_t old = atom_add_acq_rel(p.cnt_sample + i, 1u);  // release: the masses above
       sm.last = (old + 1u == static_cast<uint32_t>(NC)) ? 1 : 0;
-      __threadfence();
     }
     __syncthreads();
     if (!sm.last) return;
+    if (tid == 0) p.cnt_sample[i] = 0;
+    // one round for every chunk mass and every warp-range mass of the request
+    if (stage_mass) {
+      for (int j = tid; j < NC; j += kSampleThreads) mass_s[j] = __ldcg(p.mass + static_cast<int64_t>(i) * NC + j);
+      for (int j = tid; j < NC * kSampleWarps; j += kSampleThreads) mass_s[NC + j] = __ldcg(wm + j);
+    }
+    __syncthreads();
   }
 
-  // ---- one CTA per request from here on ----
-  if (tid == 0) {
-    sm.flags = 0;
-    sm.use_bonus_row = residual ? 0 : 1;
-    double Z = 0.0;
-    if (residual) {
-      for (int cc = 0; cc < NC; ++cc) Z += static_cast<double>(__ldcg(p.mass + static_cast<int64_t>(i) * NC + cc));
-      if (!(Z > 0.0)) {
-        sm.flags |= SV_FLAG_Z_ZERO;
-        sm.use_bonus_row = 1;  // draw from p_a instead
+  // one CTA per request from here on: find the crossing chunk
+  if (warp == 0) {
+    const float* mass_g = p.mass + static_cast<int64_t>(i) * NC;
+    auto mass_at = [&](int cc) { return stage_mass ? mass_s[cc] : __ldcg(mass_g + cc); };
+    const ChunkRecord* rr = recs + static_cast<int64_t>(st.rec_row_t) * NC;
+    int bonus = st.mode == kModeBonus ? 1 : 0;
+    uint32_t flags = 0;
+    float Z = 0.0f;
+    if (!bonus) {
+      for (int cc = lane; cc < NC; cc += 32) Z += mass_at(cc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
+      if (!(Z > 0.0f)) {
+        bonus = 1;  // residual mass 0 (not reachable in exact arithmetic): draw from p_a
+        flags |= SV_FLAG_Z_ZERO;
       }
     }
-    if (sm.use_bonus_row) {
-      Z = 0.0;
-      const ChunkRecord* rr = p.rec + static_cast<int64_t>(st.rec_row_t) * NC;
-      for (int cc = 0; cc < NC; ++cc) {
-        const ChunkRecord rc = ld_record(rr + cc);
-        if (rc.m != -INFINITY)
-          Z += static_cast<double>(rc.s) * static_cast<double>(exp2f((rc.m - st.mt) * st.kscale));
-      }
+    // the staged records are intact unless the residual path reused their space for masses
+    const bool recs_intact = FL.staged && !(st.mode == kModeResidual && stage_mass);
+    auto rec_w = [&](int cc) -> float {
+      const ChunkRecord rc = recs_intact ? rr[cc] : ld_record(rec_g + static_cast<int64_t>(st.rec_row_t) * NC + cc);
+      return rc.m == -INFINITY ? 0.0f : rc.s * exp2f((rc.m - st.mt) * st.kscale);
+    };
+    if (bonus) {
+      Z = 0.0f;
+      for (int cc = lane; cc < NC; cc += 32) Z += rec_w(cc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
     }
-    const double thr = st.u * Z;
-    double base = 0.0;
-    int cstar = -1;
-    int last_pos_chunk = -1;
-    for (int cc = 0; cc < NC; ++cc) {
-      double w;
-      if (sm.use_bonus_row) {
-        const ChunkRecord rc = ld_record(p.rec + static_cast<int64_t>(st.rec_row_t) * NC + cc);
-        w = rc.m != -INFINITY ? static_cast<double>(rc.s) * static_cast<double>(exp2f((rc.m - st.mt) * st.kscale)) : 0.0;
-      } else {
-        w = static_cast<double>(__ldcg(p.mass + static_cast<int64_t>(i) * NC + cc));
-      }
-      if (w > 0.0) last_pos_chunk = cc;
-      if (base + w > thr && w > 0.0) {
-        cstar = cc;
-        break;
-      }
-      base += w;
+    const float thr = st.u * Z;
+    float before = 0.0f;
+    int cstar;
+    if (bonus) cstar = warp_find(NC, thr, rec_w, &before, lane);
+    else cstar = warp_find(NC, thr, mass_at, &before, lane);
+    if (lane == 0) {
+      sm.chunk = cstar;
+      sm.base = before;
+      sm.thr = thr;
+      sm.bonus = bonus;
+      sm.flags = flags;
     }
-    if (cstar < 0) {  // rounding pushed the threshold past the end: last chunk with mass
-      cstar = last_pos_chunk < 0 ? 0 : last_pos_chunk;
-      base = thr;     // pick the first positive weight of that chunk
-    }
-    sm.chunk = cstar;
-    sm.base = base;
-    sm.Z = Z;
   }
   __syncthreads();
-  residual = !sm.use_bonus_row;
   const int cstar = sm.chunk;
+  const bool residual = !sm.bonus;
   const int c0 = cstar * p.chunk_len, len = min(p.chunk_len, p.V - c0);
-  stage_chunk<DT>(tbuf, row_ptr<DT>(p.target, st.row_t, p.t_row_stride) + static_cast<int64_t>(c0) * kElt, len, tid);
-  if (residual)
-    stage_chunk<DT>(dbuf, row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) + static_cast<int64_t>(c0) * kElt, len, tid);
-  __syncthreads();
-  const double thr = st.u * sm.Z;
-  // when the chunk search fell off the end, base == thr: any positive weight crosses
-  const int yloc = scan_pick<DT>(tbuf, dbuf, len, residual, st, sm.base, thr, tid, &sm);
-  if (tid == 0) {
-    // yloc < 0 only if every weight of the chosen chunk flushed to zero (a chunk mass below the
-    // float range); keep the output a valid token.
-    const int y = c0 + (yloc >= 0 ? yloc : 0);
-    p.out_tokens[static_cast<int64_t>(i) * (p.Kmax + 1) + st.a] = y;
-    if (p.out_flags && sm.flags) p.out_flags[i] = static_cast<uint8_t>(st.flags | sm.flags);
-    if (residual || st.mode == kModeResidual) p.cnt_sample[i] = 0;
+  const char* dr = residual ? drow : trow;
+
+  // the crossing warp range inside the chunk
+  if (!residual) {  // masses of the target row's warp ranges are recomputed here
+    int lo, hi;
+    warp_range(len, warp, &lo, &hi);
+    const float ws = warp_range_sum<DT>(trow, trow, c0, lo, hi, false, st, lane);
+    if (lane == 0) sm.wsum[warp] = ws;
+    __syncthreads();
+  }
+  if (warp == 0) {
+    float before = 0.0f;
+    const float rem = sm.thr - sm.base;
+    auto wr = [&](int j) {
+      if (!residual) return sm.wsum[j];
+      return stage_mass ? mass_s[NC + cstar * kSampleWarps + j] : __ldcg(wm + cstar * kSampleWarps + j);
+    };
+    const int w = warp_find(kSampleWarps, rem, wr, &before, lane);
+    int lo, hi;
+    warp_range(len, w, &lo, &hi);
+    int y = warp_pick<DT>(trow, dr, c0, lo, hi, residual, st, sm.base + before, sm.thr, lane, sm.wbuf);
+    if (y < 0) y = lo;  // only if every weight of the range flushed to zero; keep a valid token
+    if (lane == 0) {
+      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + y;
+      if (p.out_flags && sm.flags) p.out_flags[i] = static_cast<uint8_t>(st.flags | sm.flags);
+    }
   }
 }
 
-int g_stats_blocks_per_sm[2] = {0, 0};
+bool g_stats_attr_set[2] = {false, false};
+bool g_fin_attr_set[2] = {false, false};
 int g_num_sms = 0;
 
 template <int DT>
 cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
-  const size_t dyn = static_cast<size_t>(kStages) * kStageBytes + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
+  const size_t table = static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
+  const size_t dyn = static_cast<size_t>(kStages) * kStageBytes + table;
   cudaError_t e;
   if (g_num_sms == 0) {
     int dev;
@@ -787,43 +1097,45 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
     if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   }
   const int di = DT == SV_BF16 ? 0 : 1;
-  {
-    const size_t max_dyn = static_cast<size_t>(kStages) * kStageBytes + SV_MAX_BATCH * 2;
-    if (g_stats_blocks_per_sm[di] == 0) {
-      if ((e = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(max_dyn))) != cudaSuccess)
-        return e;
-      int nb = 0;
-      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, row_stats_kernel<DT>, kStatsThreads,
-                                                             static_cast<size_t>(kStages) * kStageBytes + 1024)) != cudaSuccess)
-        return e;
-      g_stats_blocks_per_sm[di] = nb > 0 ? nb : 1;
-    }
+  if (!g_stats_attr_set[di]) {
+    const size_t max_dyn = static_cast<size_t>(kStages) * kStageBytes + (SV_MAX_BATCH + 4) * 4 + SV_MAX_BATCH * 2;
+    if ((e = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(max_dyn))) != cudaSuccess)
+      return e;
+    g_stats_attr_set[di] = true;
   }
+  int nb = 0;  // resident CTAs per SM at this table size (the grid is persistent)
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, row_stats_kernel<DT>, kStatsThreads, dyn)) != cudaSuccess)
+    return e;
   const int64_t slots = static_cast<int64_t>(p.B) * p.rows_per_req * p.nchunks;
-  const int64_t cap = static_cast<int64_t>(g_num_sms) * g_stats_blocks_per_sm[di];
+  const int64_t cap = static_cast<int64_t>(g_num_sms) * (nb > 0 ? nb : 1);
   const int grid = static_cast<int>(slots < cap ? slots : cap);
   prof_before(SV_KERNEL_ROW_STATS, stream);
   row_stats_kernel<DT><<<grid, kStatsThreads, dyn, stream>>>(p);
   prof_after(SV_KERNEL_ROW_STATS, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (!sampled) return cudaSuccess;
 
+  if (!g_fin_attr_set[di]) {
+    if ((e = cudaFuncSetAttribute(finalize_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kFinMaxDynSmem)) != cudaSuccess)
+      return e;
+    g_fin_attr_set[di] = true;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.B), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(sampled ? p.nchunks : 1), static_cast<unsigned>(p.B), 1);
   cfg.blockDim = dim3(kSampleThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  // Programmatic dependent launch lets the sample grid's launch overlap the row_stats tail; it
-  // is left out while instrumentation puts an event between the two kernels.
+  // Programmatic dependent launch lets the finalize grid's launch overlap the row_stats tail;
+  // it is left out while instrumentation puts an event between the two kernels.
   cfg.numAttrs = prof_enabled() ? 0 : 1;
-  prof_before(SV_KERNEL_SAMPLE, stream);
-  e = cudaLaunchKernelEx(&cfg, sample_kernel<DT>, p);
-  prof_after(SV_KERNEL_SAMPLE, stream);
+  prof_before(SV_KERNEL_FINALIZE, stream);
+  e = cudaLaunchKernelEx(&cfg, finalize_kernel<DT>, p);
+  prof_after(SV_KERNEL_FINALIZE, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -851,16 +1163,12 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   size_t off = 0;
   L.status = off;
   off = align256(off + 256);
-  L.cnt_stats = off;
-  off = align256(off + sizeof(uint32_t) * B);
   L.cnt_sample = off;
   off = align256(off + sizeof(uint32_t) * B);
-  L.req = off;
-  off = align256(off + sizeof(ReqState) * B);
-  L.rowstat = off;
-  off = align256(off + sizeof(RowStat) * B * R);
   L.mass = off;
   off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
+  L.wmass = off;
+  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks) * kSampleWarps);
   L.rec = off;
   off = align256(off + sizeof(ChunkRecord) * B * R * static_cast<size_t>(nchunks));
   L.total = off;
