@@ -214,6 +214,35 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
                             int32_t* out_row_offsets, int32_t* out_total_K,
                             int64_t* out_utility_q48, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * sv_verify_sample_noalloc -- sv_verify_sample without a caller workspace.  The AngelSpec
+ * pages have no counterpart to this call; it exists for callers that cannot call cudaMalloc:
+ * code that runs while its stream is being captured into a CUDA graph (an allocation there
+ * would break the capture), plugins inside a host framework whose device memory belongs to
+ * that framework's own allocator, and serving loops that allow no allocation on the hot path
+ * (cudaMalloc can synchronize the whole device).
+ *
+ * Arguments and results are those of sv_verify_sample, without ws / ws_bytes; the caller
+ * still passes every input and output.  The scratch is an array of SV_NOALLOC_SCRATCH_BYTES
+ * (4 MiB) inside the library, held on every GPU that loads the library until the process
+ * exits.  A call whose sv_workspace_size(SV_OP_VERIFY, B, K, V, dt) exceeds it returns
+ * SV_ERR_WORKSPACE (message in sv_last_error_string) and enqueues nothing.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture.  Each call clears the start of the array
+ * (status word and draw counters) with cudaMemsetAsync on `stream`.  All calls share the one
+ * array: calls that may overlap on the GPU (different streams of one device) race.  Nothing
+ * is allocated: no cudaMalloc, cudaFree or allocating library routine.  Input errors that
+ * only the kernels see are reported through out_accept_len = -1 and out_flags
+ * (SV_FLAG_INVALID); there is no status word to query.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
+sv_status sv_verify_sample_noalloc(const void* target, int64_t t_row_stride, const void* draft,
+                                   int64_t d_row_stride, const int32_t* draft_tokens,
+                                   const float* temperature, uint64_t seed, uint32_t round,
+                                   const int32_t* request_ids, sv_dtype dt, int B, int K, int V,
+                                   int32_t* out_tokens, int32_t* out_accept_len, float* out_p,
+                                   float* out_q, uint8_t* out_flags, void* stream);
+
 /* Synchronizes `stream`, returns the workspace's device status word in
  * *device_status (SV_DEV_* bits) and clears it.  Returns SV_OK if the word was
  * zero, SV_ERR_TIMEOUT if SV_DEV_TIMEOUT is set, else SV_ERR_DEVICE_INPUT. */

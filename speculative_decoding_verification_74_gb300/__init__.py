@@ -44,6 +44,8 @@ _SIGS = {
     "sv_verify_ragged": (_c.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _c.c_int, _vp, _vp, _u64, _u32,
                                     _vp, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp,
                                     _vp, _sz, _vp]),
+    "sv_verify_sample_noalloc": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _u64, _u32, _vp, _c.c_int,
+                                            _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sv_schedule_depth": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _f32, _f32, _c.c_int, _vp,
                                      _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sv_query_status": (_c.c_int, [_vp, _vp, _c.POINTER(_u32)]),
@@ -148,6 +150,16 @@ def sv_verify_ragged(target, t_row_stride, t_row_offsets, draft, d_row_stride, d
                                   _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B, Kmax,
                                   V, _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q), _p(out_flags),
                                   _p(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def sv_verify_sample_noalloc(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round_,
+                             request_ids, dt, B, K, V, out_tokens, out_accept_len, out_p, out_q, out_flags,
+                             stream=None) -> None:
+    """sv_verify_sample on the library's built-in scratch (no workspace argument)."""
+    _check(lib().sv_verify_sample_noalloc(_p(target), t_row_stride, _p(draft), d_row_stride, _p(draft_tokens),
+                                          _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B,
+                                          K, V, _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q),
+                                          _p(out_flags), _stream(stream)))
 
 
 def sv_schedule_depth(alpha, alpha_stride, draft_len, B, Dmax, cost_a, cost_b, budget, ratios, objective,

@@ -125,6 +125,22 @@ void record(cudaEvent_t e, cudaStream_t s) {
 }  // namespace
 
 namespace sv {
+sv_status validate_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                          const int32_t* draft_tokens, const float* temperature, sv_dtype dt, int B, int K, int V,
+                          const int32_t* out_tokens, const int32_t* out_accept_len) {
+  sv_status s = check_common(target, t_row_stride, draft, d_row_stride, dt, B, K, V, out_tokens, out_accept_len);
+  if (s != SV_OK) return s;
+  if (B > 0 && (temperature == nullptr || (K > 0 && draft_tokens == nullptr)))
+    return fail(SV_ERR_INVALID_ARG, "sampled verification needs temperature and draft_tokens");
+  return SV_OK;
+}
+sv_status set_error(sv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
 bool prof_enabled() { return g_prof_on; }
 void prof_before(int id, void* stream) {
   if (!g_prof_on) return;
@@ -187,10 +203,9 @@ sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void*
                            const int32_t* request_ids, sv_dtype dt, int B, int K, int V, int32_t* out_tokens,
                            int32_t* out_accept_len, float* out_p, float* out_q, uint8_t* out_flags, void* ws,
                            size_t ws_bytes, void* stream) {
-  sv_status s = check_common(target, t_row_stride, draft, d_row_stride, dt, B, K, V, out_tokens, out_accept_len);
+  sv_status s = sv::validate_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, dt, B, K,
+                                    V, out_tokens, out_accept_len);
   if (s != SV_OK) return s;
-  if (B > 0 && (temperature == nullptr || (K > 0 && draft_tokens == nullptr)))
-    return fail(SV_ERR_INVALID_ARG, "sampled verification needs temperature and draft_tokens");
   sv::VerifyParams p = {};
   p.target = target;
   p.t_row_stride = t_row_stride;

@@ -104,6 +104,14 @@ void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);
 int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream);
 int launch_schedule(const ScheduleParams& p, void* stream);
 
+// Host-side argument checks of sv_verify_sample (sv_api.cu); touch no GPU.
+sv_status validate_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                          const int32_t* draft_tokens, const float* temperature, sv_dtype dt, int B, int K, int V,
+                          const int32_t* out_tokens, const int32_t* out_accept_len);
+
+// Records the message returned by sv_last_error_string and returns s (sv_api.cu).
+sv_status set_error(sv_status s, const char* fmt, ...);
+
 // Instrumentation hooks implemented in sv_api.cu.
 bool prof_enabled();
 void prof_before(int kernel_id, void* stream);
