@@ -80,11 +80,16 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
   p.chunk_len = cl;
   p.nchunks = nc;
   p.rows_per_req = 2 * p.Kmax + 1;
+  // Fixed-K calls need no per-request plan: every request has the same rows.
+  if (p.keep_len == nullptr && p.t_off == nullptr && p.d_off == nullptr) {
+    const bool drafts = p.temperature == nullptr ? p.tokens == nullptr : p.draft != nullptr;
+    p.uniform_rows = drafts ? 2 * p.Kmax + 1 : p.Kmax + 1;
+  }
   p.status = reinterpret_cast<uint32_t*>(w + L.status);
   p.cnt_sample = reinterpret_cast<uint32_t*>(w + L.cnt_sample);
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
-  p.wmass = reinterpret_cast<float*>(w + L.wmass);
+  p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
   const int e = sv::launch_verify(p, dt, sampled, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;

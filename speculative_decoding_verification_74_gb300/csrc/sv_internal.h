@@ -72,7 +72,8 @@ struct VerifyParams {
   uint32_t* cnt_sample;     // [B] per-request counter of the draw's chunk CTAs
   ChunkRecord* rec;         // [B * rows_per_req * nchunks]
   float* mass;              // [B * nchunks] residual mass per chunk
-  float* wmass;             // [B * nchunks * kSampleWarps] residual mass per warp range
+  float* mass_p;            // [B * nchunks] target-row weight per chunk (bonus draw / fallback)
+  int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
 };
 
 struct ScheduleParams {
@@ -95,7 +96,7 @@ struct ScheduleParams {
 
 // Workspace layout for SV_OP_VERIFY.
 struct VerifyLayout {
-  size_t status, cnt_sample, rec, mass, wmass, total;
+  size_t status, cnt_sample, rec, mass, mass_p, total;
 };
 VerifyLayout verify_layout(int B, int Kmax, int nchunks);
 void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);

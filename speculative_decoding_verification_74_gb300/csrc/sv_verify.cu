@@ -165,6 +165,16 @@ __device__ __forceinline__ const char* row_base(const VerifyParams& p, const Row
                       : row_ptr<DT>(p.draft, draft_row(p, rr.i, rr.k), p.d_row_stride);
 }
 
+// Closed-form plan: every request has U record rows (its K + 1 target rows, then its K draft
+// rows when U == 2K + 1).
+__device__ __forceinline__ void locate_row_uniform(int U, int Kmax, int row, RowRef& rr) {
+  rr.i = row / U;
+  const int q = row - rr.i * U;
+  rr.is_target = q <= Kmax;
+  rr.k = rr.is_target ? q : q - Kmax - 1;
+  rr.rec_row = rr.is_target ? rr.k : Kmax + 1 + rr.k;
+}
+
 __device__ __forceinline__ int rows_of(uint16_t inf) {
   if (inf & kInfoInvalid) return 0;
   const int n = inf & kInfoN;
@@ -202,15 +212,23 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
-  // ---- prologue: per-request info and the row prefix (every CTA computes the same table) ----
-  {
+  // ---- prologue: barriers, and (ragged calls) per-request info and the row prefix ----
+  const bool uniform = p.uniform_rows > 0;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_proxy_async_smem();
+  }
+  if (!uniform) {  // every CTA computes the same table; finalize reports invalid requests
     const int per = (B + kStatsThreads - 1) / kStatsThreads;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
     int local = 0;
     for (int i = lo; i < hi; ++i) {
       uint32_t bad;
       info[i] = request_info(p, i, &bad);
-      if (bad && blockIdx.x == 0) atomicOr(p.status, bad);
       local += rows_of(info[i]);
     }
     int incl = local;
@@ -220,14 +238,6 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
       if (lane >= o) incl += y;
     }
     if (lane == 31) warp_tot[warp] = incl;
-    if (tid == 0) {
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(&full_bar[s], 1);
-        mbar_init(&empty_bar[s], kConsumerWarps);
-      }
-      abort_flag = 0;
-      fence_proxy_async_smem();
-    }
     __syncthreads();
     int base = 0;
     for (int w = 0; w < warp; ++w) base += warp_tot[w];
@@ -237,21 +247,26 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
       run += rows_of(info[i]);
     }
     if (tid == kStatsThreads - 1) row_start[B] = base + incl;
-    __syncthreads();
   }
-  const int64_t T = static_cast<int64_t>(row_start[B]) * NC;
+  __syncthreads();
+  const int64_t rows_total = uniform ? static_cast<int64_t>(B) * p.uniform_rows : row_start[B];
+  const int64_t T = rows_total * NC;
   const int64_t t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
   if (t0 >= t1) {
     pdl_trigger();
     return;
   }
+  auto locate = [&](int row, int& i, RowRef& rr) {
+    if (uniform) locate_row_uniform(p.uniform_rows, Kmax, row, rr);
+    else locate_row(row_start, info, Kmax, row, i, rr);
+  };
 
   if (tid >= kConsumerThreads) {
     // ---------------- producer warp: one lane issues the bulk copies ----------------
     if (tid == kConsumerThreads) {
       int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
       RowRef rr;
-      locate_row(row_start, info, Kmax, row, i, rr);
+      locate(row, i, rr);
       const char* src = row_base<DT>(p, rr);
       uint32_t it = 0;
       for (int64_t t = t0; t < t1; ++t) {
@@ -275,7 +290,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
         }
         if (++c == NC && t + 1 < t1) {
           c = 0;
-          locate_row(row_start, info, Kmax, ++row, i, rr);
+          locate(++row, i, rr);
           src = row_base<DT>(p, rr);
         }
       }
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   // ---------------- consumer warps ----------------
   int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
   RowRef rr;
-  locate_row(row_start, info, Kmax, row, i, rr);
+  locate(row, i, rr);
   uint32_t it = 0;
   int buf = 0;
   bool row_open = false;
@@ -304,10 +319,19 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   int g = -1, tok = -1, c_first = 0;
   for (int64_t t = t0; t < t1; ++t) {
     if (!row_open) {
-      const uint16_t inf = info[rr.i];
-      sampled = inf & kInfoSampled;
-      kscale = sampled ? kscale_of(__ldg(p.temperature + rr.i)) : 0.0f;
-      tok = (tid == 0 && sampled && rr.k < (inf & kInfoN))
+      int n;
+      if (uniform) {  // invalid temperatures give garbage statistics; finalize rejects the request
+        const float T = p.temperature ? __ldg(p.temperature + rr.i) : 0.0f;
+        sampled = T > 0.0f;
+        kscale = sampled ? kscale_of(T) : 0.0f;
+        n = Kmax;
+      } else {
+        const uint16_t inf = info[rr.i];
+        sampled = inf & kInfoSampled;
+        kscale = sampled ? kscale_of(__ldg(p.temperature + rr.i)) : 0.0f;
+        n = inf & kInfoN;
+      }
+      tok = (tid == 0 && sampled && p.tokens != nullptr && rr.k < n)
                 ? __ldg(p.tokens + static_cast<int64_t>(rr.i) * p.tok_stride + rr.k) : -1;
       rowp = row_base<DT>(p, rr);
       c_first = c;
@@ -500,7 +524,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
     }
     if (++c == NC && t + 1 < t1) {
       c = 0;
-      locate_row(row_start, info, Kmax, ++row, i, rr);
+      locate(++row, i, rr);
     }
   }
   pdl_trigger();
@@ -527,13 +551,15 @@ struct FinSmem {
   uint32_t acc_flags;
   uint32_t bad;
   float wsum[kSampleWarps];
+  float wsum_p[kSampleWarps];
   int last;
   int chunk;        // crossing chunk
   int bonus;        // draw from the target row (bonus, or residual mass 0)
   uint32_t flags;
   float base;       // mass before the crossing chunk
   float thr;        // u' * Z
-  float wbuf[kMaxRange + kMaxRange / 32];  // draw weights of the crossing warp range (skewed)
+  int pick_thread;   // first thread whose entries hold the crossing
+  int last_pos;      // broadcast of the pick
 };
 
 // weight of vocabulary entry v of a row pair for the draw (target-only when !residual)
@@ -556,11 +582,16 @@ __device__ __forceinline__ void warp_range(int len, int w, int* lo, int* hi) {
 // 16-byte vectors, so each lane issues all of its loads (<= 4 per row) before using any.
 constexpr int kRangeVecPerLane = 4;
 template <int DT>
-__device__ float warp_range_sum(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
-                                const ReqState& st, int lane) {
+__device__ void warp_range_sum(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
+                               const ReqState& st, int lane, float* sum_r, float* sum_p) {
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;
-  float acc = 0.0f;
+  float acc_r = 0.0f, acc_p = 0.0f;
+  auto add = [&](float tx, float dx) {
+    const float pv = ex2_approx((tx - st.mt) * st.kscale);
+    acc_p += pv;
+    if (residual) acc_r += fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx - st.md) * st.kscale) * st.inv_sd);
+  };
   const int len = hi - lo;
   const ChunkSplit a = split_chunk<kElt>(trow, c0 + lo, len);
   const ChunkSplit b = residual ? split_chunk<kElt>(drow, c0 + lo, len) : a;
@@ -575,87 +606,80 @@ __device__ float warp_range_sum(const char* trow, const char* drow, int c0, int 
       tw[u] = v < a.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
       dw[u] = (residual && v < a.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
     }
-    const float hx = lane < a.head ? draw_weight<DT>(trow, drow, c0 + lo + lane, residual, st) : 0.0f;
-    const float tx_ = lane < a.tail ? draw_weight<DT>(trow, drow, v0 + a.nvec * kVec + lane, residual, st) : 0.0f;
+    const bool hh = lane < a.head, ht = lane < a.tail;
+    const float hx = hh ? load_logit<DT>(trow, c0 + lo + lane) : 0.0f;
+    const float hd = (hh && residual) ? load_logit<DT>(drow, c0 + lo + lane) : 0.0f;
+    const float tx_ = ht ? load_logit<DT>(trow, v0 + a.nvec * kVec + lane) : 0.0f;
+    const float td_ = (ht && residual) ? load_logit<DT>(drow, v0 + a.nvec * kVec + lane) : 0.0f;
 #pragma unroll
     for (int u = 0; u < kRangeVecPerLane; ++u) {
       if (lane + 32 * u >= a.nvec) break;
-      float tx[kVec], dx[kVec];
       if constexpr (DT == SV_BF16) {
         const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          tx[2 * e] = bf16_lo(t4[e]);
-          tx[2 * e + 1] = bf16_hi(t4[e]);
-          dx[2 * e] = bf16_lo(d4[e]);
-          dx[2 * e + 1] = bf16_hi(d4[e]);
+          add(bf16_lo(t4[e]), bf16_lo(d4[e]));
+          add(bf16_hi(t4[e]), bf16_hi(d4[e]));
         }
       } else {
-        tx[0] = __uint_as_float(tw[u].x);
-        tx[1] = __uint_as_float(tw[u].y);
-        tx[2] = __uint_as_float(tw[u].z);
-        tx[3] = __uint_as_float(tw[u].w);
-        dx[0] = __uint_as_float(dw[u].x);
-        dx[1] = __uint_as_float(dw[u].y);
-        dx[2] = __uint_as_float(dw[u].z);
-        dx[3] = __uint_as_float(dw[u].w);
-      }
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
-        acc += residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
+        add(__uint_as_float(tw[u].x), __uint_as_float(dw[u].x));
+        add(__uint_as_float(tw[u].y), __uint_as_float(dw[u].y));
+        add(__uint_as_float(tw[u].z), __uint_as_float(dw[u].z));
+        add(__uint_as_float(tw[u].w), __uint_as_float(dw[u].w));
       }
     }
-    acc += hx + tx_;
+    if (hh) add(hx, hd);
+    if (ht) add(tx_, td_);
   } else {
-#pragma unroll 8
-    for (int e = lane; e < len; e += 32) acc += draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+#pragma unroll 4
+    for (int e = lane; e < len; e += 32)
+      add(load_logit<DT>(trow, c0 + lo + e), residual ? load_logit<DT>(drow, c0 + lo + e) : 0.0f);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
+  for (int o = 16; o > 0; o >>= 1) {
+    acc_r += __shfl_xor_sync(0xFFFFFFFFu, acc_r, o);
+    acc_p += __shfl_xor_sync(0xFFFFFFFFu, acc_p, o);
+  }
+  *sum_r = acc_r;
+  *sum_p = acc_p;
 }
 
-// Inverse-CDF pick inside [lo, hi) of a chunk (hi - lo <= kMaxRange) by one warp.  The range's
-// weights are computed once (all loads issued together) into shared memory, skewed by one slot
-// per 32 so that each lane can walk its own contiguous 32 entries without bank conflicts.
-// Returns the first v with base + cumsum > thr, or, if rounding keeps every partial sum at or
-// below thr, the last entry with positive weight (-1 if none).
+// Inverse-CDF pick inside one chunk by the whole CTA.  Thread t owns the contiguous entries
+// [t*per, (t+1)*per) of the chunk (per <= 32), loaded with 16-byte vectors when the layout allows,
+// every load issued before any is used.  Returns the chunk-relative index of the first entry with
+// cumsum > rem, or, if rounding keeps every partial sum at or below rem, the last entry with
+// positive weight (-1 if none).  Called by all threads of the CTA.
 template <int DT>
-__device__ int warp_pick(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
-                         const ReqState& st, float base, float thr, int lane, float* wbuf) {
+__device__ int block_pick(const char* trow, const char* drow, int c0, int len, bool residual, const ReqState& st,
+                          float rem, FinSmem* sm, int tid) {
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;
-  const int len = hi - lo;
-  const ChunkSplit sa = split_chunk<kElt>(trow, c0 + lo, len);
-  const ChunkSplit sb = residual ? split_chunk<kElt>(drow, c0 + lo, len) : sa;
-  if (sa.nvec > 0 && sa.head == sb.head && sa.nvec <= 32 * kRangeVecPerLane) {
-    // 16-byte vectors, every load issued before any is used
-    const int v0 = lo + sa.head;  // chunk-relative index of the first vector element
-    const uint4* tv = reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(c0 + v0) * kElt);
-    const uint4* dv = reinterpret_cast<const uint4*>(drow + static_cast<int64_t>(c0 + v0) * kElt);
-    uint4 tw[kRangeVecPerLane], dw[kRangeVecPerLane];
+  constexpr int kMaxPer = 32;
+  constexpr int kMaxV = 4;  // bf16: 32 entries, fp32: 16 entries per thread
+  const int lane = tid & 31, warp = tid >> 5;
+  const int per = (len + kSampleThreads - 1) / kSampleThreads;
+  const int a = min(len, tid * per), b = min(len, a + per);
+  const int cnt = b - a;
+  const char* tp = trow + static_cast<int64_t>(c0 + a) * kElt;
+  const char* dp = drow + static_cast<int64_t>(c0 + a) * kElt;
+  const bool vec = per % kVec == 0 && per / kVec <= kMaxV && cnt == per &&
+                   (reinterpret_cast<uintptr_t>(tp) & 15u) == 0 && (!residual || (reinterpret_cast<uintptr_t>(dp) & 15u) == 0);
+  float w[kMaxPer];
 #pragma unroll
-    for (int u = 0; u < kRangeVecPerLane; ++u) {
-      const int v = lane + 32 * u;
-      tw[u] = v < sa.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
-      dw[u] = (residual && v < sa.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
-    }
-    if (lane < sa.head) {
-      const int e = lane;
-      wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
-    }
-    if (lane < sa.tail) {
-      const int e = sa.head + sa.nvec * kVec + lane;
-      wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+  for (int j = 0; j < kMaxPer; ++j) w[j] = 0.0f;
+  if (vec) {
+    const int nv = per / kVec;
+    uint4 tv[kMaxV], dv[kMaxV];
+#pragma unroll
+    for (int u = 0; u < kMaxV; ++u) {
+      tv[u] = u < nv ? __ldg(reinterpret_cast<const uint4*>(tp) + u) : make_uint4(0, 0, 0, 0);
+      dv[u] = (residual && u < nv) ? __ldg(reinterpret_cast<const uint4*>(dp) + u) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kRangeVecPerLane; ++u) {
-      const int v = lane + 32 * u;
-      if (v >= sa.nvec) break;
+    for (int u = 0; u < kMaxV; ++u) {
       float tx[kVec], dx[kVec];
       if constexpr (DT == SV_BF16) {
-        const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
+        const uint32_t t4[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w}, d4[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           tx[2 * e] = bf16_lo(t4[e]);
@@ -664,69 +688,68 @@ __device__ int warp_pick(const char* trow, const char* drow, int c0, int lo, int
           dx[2 * e + 1] = bf16_hi(d4[e]);
         }
       } else {
-        tx[0] = __uint_as_float(tw[u].x);
-        tx[1] = __uint_as_float(tw[u].y);
-        tx[2] = __uint_as_float(tw[u].z);
-        tx[3] = __uint_as_float(tw[u].w);
-        dx[0] = __uint_as_float(dw[u].x);
-        dx[1] = __uint_as_float(dw[u].y);
-        dx[2] = __uint_as_float(dw[u].z);
-        dx[3] = __uint_as_float(dw[u].w);
+        tx[0] = __uint_as_float(tv[u].x);
+        tx[1] = __uint_as_float(tv[u].y);
+        tx[2] = __uint_as_float(tv[u].z);
+        tx[3] = __uint_as_float(tv[u].w);
+        dx[0] = __uint_as_float(dv[u].x);
+        dx[1] = __uint_as_float(dv[u].y);
+        dx[2] = __uint_as_float(dv[u].z);
+        dx[3] = __uint_as_float(dv[u].w);
       }
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
-        const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
-        const float w =
-            residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
-        const int idx = sa.head + v * kVec + e;  // range-relative element
-        wbuf[idx + (idx >> 5)] = w;
+        const int j = u * kVec + e;
+        if (j < kMaxPer) {
+          const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
+          w[j] = (j < cnt) ? (residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd)
+                                       : pv)
+                           : 0.0f;
+        }
       }
     }
   } else {
-#pragma unroll 8
-    for (int e = lane; e < len; e += 32) wbuf[e + (e >> 5)] = draw_weight<DT>(trow, drow, c0 + lo + e, residual, st);
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j)
+      if (j < cnt) w[j] = draw_weight<DT>(trow, drow, c0 + a + j, residual, st);
   }
-  __syncwarp();
-  const int a = min(len, lane * 32), b = min(len, a + 32);
-  float ssum = 0.0f;
+  float sum = 0.0f;
   int lastpos = -1;
-  for (int e = a; e < b; ++e) {
-    const float w = wbuf[e + (e >> 5)];
-    ssum += w;
-    if (w > 0.0f) lastpos = e;
+#pragma unroll
+  for (int j = 0; j < kMaxPer; ++j) {
+    sum += w[j];
+    if (w[j] > 0.0f) lastpos = a + j;
   }
-  float incl = ssum;
+  // block exclusive scan of the per-thread sums
+  float incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += y;
   }
-  const float excl = incl - ssum;
-  const float rem = thr - base;
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, b > a && ssum > 0.0f && excl + ssum > rem);
-  int y = -1;
-  if (hit) {
-    const int src = __ffs(hit) - 1;
-    if (lane == src) {
-      float run = excl;
-      for (int e = a; e < b; ++e) {
-        const float w = wbuf[e + (e >> 5)];
-        run += w;
-        if (w > 0.0f && run > rem) {
-          y = e;
-          break;
-        }
-      }
-      if (y < 0) y = lastpos;
-    }
-    y = __shfl_sync(0xFFFFFFFFu, y, src);
-  } else {
-    int lp = lastpos;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
-    y = lp;
+  if (lane == 31) sm->wsum[warp] = incl;
+  if (tid == 0) {
+    sm->pick_thread = kSampleThreads;
+    sm->last_pos = -1;
   }
-  return y < 0 ? -1 : lo + y;
+  __syncthreads();
+  float excl = incl - sum;
+  for (int v = 0; v < warp; ++v) excl += sm->wsum[v];
+  if (cnt > 0 && sum > 0.0f && excl + sum > rem) atomicMin(&sm->pick_thread, tid);
+  if (lastpos >= 0) atomicMax(&sm->last_pos, lastpos);
+  __syncthreads();
+  if (tid == sm->pick_thread) {
+    float run = excl;
+    int y = -1;
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+      run += w[j];
+      if (y < 0 && w[j] > 0.0f && run > rem) y = a + j;
+    }
+    sm->last_pos = y >= 0 ? y : lastpos;
+  }
+  __syncthreads();
+  return sm->last_pos;
 }
 
 // First index j in [0, cnt) whose running sum of w(j) (float, index order) exceeds thr, found by
@@ -811,13 +834,16 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   if (toks)
     for (int j = tid; j < Kmax; j += kSampleThreads) cp_async4(tok_s + j, toks + j);
   uint32_t bad_in;
-  const uint16_t info = request_info(p, i, &bad_in);  // row_stats' CTA 0 reported bad_in already
+  const uint16_t info = request_info(p, i, &bad_in);
   const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
   const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
   cp_async_wait_all();
   __syncthreads();
   if (info & kInfoInvalid) {
-    if (c == 0) write_invalid(p, i, tid, kSampleThreads);
+    if (c == 0) {
+      if (tid == 0) atomicOr(p.status, bad_in);
+      write_invalid(p, i, tid, kSampleThreads);
+    }
     return;
   }
   const int n = info & kInfoN;
@@ -947,7 +973,6 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   }
   if (!sampled) return;
   const int mode = a < n ? kModeResidual : kModeBonus;
-  if (mode == kModeBonus && c != 0) return;
   if (tid == 0) {
     ReqState st = {};
     st.mode = mode;
@@ -970,53 +995,59 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   __syncthreads();
 
   // ---------------- draw at position a ----------------
+  // Every CTA of the request sums its chunk: the residual max(0, p_a - q_a) after a rejection,
+  // and the target weights of row a (the bonus draw, or the fallback when the residual mass is
+  // zero).  The request's last CTA then finds the crossing chunk and entry.
   const ReqState& st = sm.st;
+  const bool residual_mode = st.mode == kModeResidual;
   const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
-  const char* drow = st.mode == kModeResidual ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
-  float* wm = p.wmass + static_cast<int64_t>(i) * NC * kSampleWarps;
+  const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
   float* mass_s = reinterpret_cast<float*>(fin_dyn + FL.rec_off);  // reuses the staged records' space
-  const bool stage_mass = FL.staged && static_cast<size_t>(NC) * (kSampleWarps + 1) * 4 <=
-                                           static_cast<size_t>(R) * NC * sizeof(ChunkRecord);
-
-  if (st.mode == kModeResidual) {
-    // this CTA's chunk: per-warp-range and per-chunk residual masses
+  const bool stage_mass = FL.staged && static_cast<size_t>(NC) * 8 <= static_cast<size_t>(R) * NC * sizeof(ChunkRecord);
+  float* mass_r = p.mass + static_cast<int64_t>(i) * NC;
+  float* mass_p = p.mass_p + static_cast<int64_t>(i) * NC;
+  {
     const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
     int lo, hi;
     warp_range(len, warp, &lo, &hi);
-    const float ws = warp_range_sum<DT>(trow, drow, c0, lo, hi, true, st, lane);
+    float wr, wp;
+    warp_range_sum<DT>(trow, drow, c0, lo, hi, residual_mode, st, lane, &wr, &wp);
     if (lane == 0) {
-      sm.wsum[warp] = ws;
-      __stcg(wm + c * kSampleWarps + warp, ws);
+      sm.wsum[warp] = wr;
+      sm.wsum_p[warp] = wp;
     }
     __syncthreads();
     if (tid == 0) {
-      float tot = 0.0f;
-      for (int w = 0; w < kSampleWarps; ++w) tot += sm.wsum[w];
-      __stcg(p.mass + static_cast<int64_t>(i) * NC + c, tot);
+      float tr = 0.0f, tp = 0.0f;
+      for (int w = 0; w < kSampleWarps; ++w) {
+        tr += sm.wsum[w];
+        tp += sm.wsum_p[w];
+      }
+      __stcg(mass_r + c, tr);
+      __stcg(mass_p + c, tp);
       const uint32_t old = atom_add_acq_rel(p.cnt_sample + i, 1u);  // release: the masses above
       sm.last = (old + 1u == static_cast<uint32_t>(NC)) ? 1 : 0;
     }
     __syncthreads();
     if (!sm.last) return;
     if (tid == 0) p.cnt_sample[i] = 0;
-    // one round for every chunk mass and every warp-range mass of the request
-    if (stage_mass) {
-      for (int j = tid; j < NC; j += kSampleThreads) mass_s[j] = __ldcg(p.mass + static_cast<int64_t>(i) * NC + j);
-      for (int j = tid; j < NC * kSampleWarps; j += kSampleThreads) mass_s[NC + j] = __ldcg(wm + j);
-    }
+    if (stage_mass)  // one round for every chunk mass of the request
+      for (int j = tid; j < NC; j += kSampleThreads) {
+        mass_s[j] = __ldcg(mass_r + j);
+        mass_s[NC + j] = __ldcg(mass_p + j);
+      }
     __syncthreads();
   }
 
   // one CTA per request from here on: find the crossing chunk
   if (warp == 0) {
-    const float* mass_g = p.mass + static_cast<int64_t>(i) * NC;
-    auto mass_at = [&](int cc) { return stage_mass ? mass_s[cc] : __ldcg(mass_g + cc); };
-    const ChunkRecord* rr = recs + static_cast<int64_t>(st.rec_row_t) * NC;
-    int bonus = st.mode == kModeBonus ? 1 : 0;
+    auto r_at = [&](int cc) { return stage_mass ? mass_s[cc] : __ldcg(mass_r + cc); };
+    auto p_at = [&](int cc) { return stage_mass ? mass_s[NC + cc] : __ldcg(mass_p + cc); };
+    int bonus = residual_mode ? 0 : 1;
     uint32_t flags = 0;
     float Z = 0.0f;
     if (!bonus) {
-      for (int cc = lane; cc < NC; cc += 32) Z += mass_at(cc);
+      for (int cc = lane; cc < NC; cc += 32) Z += r_at(cc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
       if (!(Z > 0.0f)) {
@@ -1024,23 +1055,15 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
         flags |= SV_FLAG_Z_ZERO;
       }
     }
-    // the staged records are intact unless the residual path reused their space for masses
-    const bool recs_intact = FL.staged && !(st.mode == kModeResidual && stage_mass);
-    auto rec_w = [&](int cc) -> float {
-      const ChunkRecord rc = recs_intact ? rr[cc] : ld_record(rec_g + static_cast<int64_t>(st.rec_row_t) * NC + cc);
-      return rc.m == -INFINITY ? 0.0f : rc.s * exp2f((rc.m - st.mt) * st.kscale);
-    };
     if (bonus) {
       Z = 0.0f;
-      for (int cc = lane; cc < NC; cc += 32) Z += rec_w(cc);
+      for (int cc = lane; cc < NC; cc += 32) Z += p_at(cc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
     }
     const float thr = st.u * Z;
     float before = 0.0f;
-    int cstar;
-    if (bonus) cstar = warp_find(NC, thr, rec_w, &before, lane);
-    else cstar = warp_find(NC, thr, mass_at, &before, lane);
+    const int cstar = bonus ? warp_find(NC, thr, p_at, &before, lane) : warp_find(NC, thr, r_at, &before, lane);
     if (lane == 0) {
       sm.chunk = cstar;
       sm.base = before;
@@ -1055,30 +1078,12 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   const int c0 = cstar * p.chunk_len, len = min(p.chunk_len, p.V - c0);
   const char* dr = residual ? drow : trow;
 
-  // the crossing warp range inside the chunk
-  if (!residual) {  // masses of the target row's warp ranges are recomputed here
-    int lo, hi;
-    warp_range(len, warp, &lo, &hi);
-    const float ws = warp_range_sum<DT>(trow, trow, c0, lo, hi, false, st, lane);
-    if (lane == 0) sm.wsum[warp] = ws;
-    __syncthreads();
-  }
-  if (warp == 0) {
-    float before = 0.0f;
-    const float rem = sm.thr - sm.base;
-    auto wr = [&](int j) {
-      if (!residual) return sm.wsum[j];
-      return stage_mass ? mass_s[NC + cstar * kSampleWarps + j] : __ldcg(wm + cstar * kSampleWarps + j);
-    };
-    const int w = warp_find(kSampleWarps, rem, wr, &before, lane);
-    int lo, hi;
-    warp_range(len, w, &lo, &hi);
-    int y = warp_pick<DT>(trow, dr, c0, lo, hi, residual, st, sm.base + before, sm.thr, lane, sm.wbuf);
-    if (y < 0) y = lo;  // only if every weight of the range flushed to zero; keep a valid token
-    if (lane == 0) {
-      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + y;
-      if (p.out_flags && sm.flags) p.out_flags[i] = static_cast<uint8_t>(st.flags | sm.flags);
-    }
+  // the crossing entry inside the chunk (the whole CTA)
+  int y = block_pick<DT>(trow, dr, c0, len, residual, st, sm.thr - sm.base, &sm, tid);
+  if (tid == 0) {
+    if (y < 0) y = 0;  // only if every weight of the chunk flushed to zero; keep a valid token
+    p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + y;
+    if (p.out_flags && sm.flags) p.out_flags[i] = static_cast<uint8_t>(st.flags | sm.flags);
   }
 }
 
@@ -1088,7 +1093,8 @@ int g_num_sms = 0;
 
 template <int DT>
 cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
-  const size_t table = static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
+  const size_t table =
+      p.uniform_rows > 0 ? 0 : static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
   const size_t dyn = static_cast<size_t>(kStages) * kStageBytes + table;
   cudaError_t e;
   if (g_num_sms == 0) {
@@ -1167,8 +1173,8 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   off = align256(off + sizeof(uint32_t) * B);
   L.mass = off;
   off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
-  L.wmass = off;
-  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks) * kSampleWarps);
+  L.mass_p = off;
+  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
   L.rec = off;
   off = align256(off + sizeof(ChunkRecord) * B * R * static_cast<size_t>(nchunks));
   L.total = off;

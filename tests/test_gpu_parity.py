@@ -282,3 +282,19 @@ def test_gpu_emissions_follow_the_target_distribution():
     assert chisquare(first, p0 * n).pvalue > 1e-4
     lens = np.asarray(lens, float)
     assert abs(lens.mean() - expected_accept_len(betas)) < 4.5 * lens.std() / np.sqrt(n)
+
+
+def test_draws_over_multi_chunk_pieces():
+    """Enough (row, chunk) tasks that each row_stats CTA covers several chunks of a row; half
+    the requests have draft = target (every drafted token accepted: bonus draws), half reject
+    (residual draws)."""
+    b = W.make_batch("pieces", ["chat"] * 12, [3] * 12, [1.0] * 12, 151936, "bf16", 42, 0, {"chat": (3.0, 1.0)})
+    for i in range(0, b.B, 2):
+        b.draft[b.d_offsets[i]: b.d_offsets[i] + 3] = b.target[b.t_offsets[i]: b.t_offsets[i] + 3]
+    out = run_ragged(b)
+    assert np.all(out[1][::2] == 3)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+    tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, "bf16"), dev_rows(b.draft, "bf16"), i32(b.tokens),
+                                           f32(b.temperature), 3, seed=b.seed, round_=b.round)
+    torch.cuda.synchronize()
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len)
