@@ -261,7 +261,14 @@ const char* sv_last_error_string(void);
  * launches[kernel id] (arrays of SV_NUM_KERNELS).  sv_profile_reset forgets the
  * brackets.  sv_launch_count returns the number of library kernel launches (or
  * captured launch nodes) since the library was loaded. */
-enum { SV_KERNEL_ROW_STATS = 0, SV_KERNEL_FINALIZE = 1, SV_KERNEL_SCHEDULE = 2, SV_NUM_KERNELS = 3 };
+enum {
+  SV_KERNEL_ROW_STATS = 0,
+  SV_KERNEL_COMBINE = 1,
+  SV_KERNEL_SCHEDULE = 2,
+  SV_KERNEL_MASS = 3,
+  SV_KERNEL_PICK = 4,
+  SV_NUM_KERNELS = 5
+};
 void sv_profile_enable(int on);
 sv_status sv_profile_collect(double* total_ms, int64_t* launches);
 void sv_profile_reset(void);

@@ -27,8 +27,8 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, S
 SV_BF16, SV_F32 = 0, 1
 SV_OP_VERIFY, SV_OP_SCHEDULE = 0, 1
 SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
-SV_KERNEL_ROW_STATS, SV_KERNEL_FINALIZE, SV_KERNEL_SCHEDULE, SV_NUM_KERNELS = 0, 1, 2, 3
-KERNEL_NAMES = ("row_stats", "finalize", "schedule")
+SV_KERNEL_ROW_STATS, SV_KERNEL_COMBINE, SV_KERNEL_SCHEDULE, SV_KERNEL_MASS, SV_KERNEL_PICK, SV_NUM_KERNELS = range(6)
+KERNEL_NAMES = ("row_stats", "combine", "schedule", "mass", "pick")
 
 _c = ctypes
 _vp, _i32, _i64, _u32, _u64, _f32, _sz = (_c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_uint64,

@@ -86,7 +86,7 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
     p.uniform_rows = drafts ? 2 * p.Kmax + 1 : p.Kmax + 1;
   }
   p.status = reinterpret_cast<uint32_t*>(w + L.status);
-  p.cnt_sample = reinterpret_cast<uint32_t*>(w + L.cnt_sample);
+  p.req = reinterpret_cast<sv::ReqState*>(w + L.req);
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
   p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
@@ -307,7 +307,7 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
   }
   sv_status s = check_ws(ws, ws_bytes, 256);
   if (s != SV_OK) return s;
-  int P = 1;
+  int P = 1024;  // the sort holds at least one key per thread
   while (P < B * Dmax) P <<= 1;
   p.alpha = alpha;
   p.alpha_stride = alpha_stride;

@@ -16,9 +16,6 @@ constexpr int kStatsThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;  // 16-byte vectors per thread
 static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split");
 
-// ---- sample kernel geometry ------------------------------------------------------------------
-constexpr int kSampleThreads = 256;
-constexpr int kSampleWarps = kSampleThreads / 32;
 
 // Per-(row, chunk) statistics written by row_stats.
 struct alignas(16) ChunkRecord {
@@ -28,7 +25,8 @@ struct alignas(16) ChunkRecord {
   float xval;  // logit at the row's drafted token, when that token lies in the chunk
 };
 
-// What the draw at the accepted length needs (kept in shared memory by the finalize kernel).
+// What the draw at the accepted length needs (written by the combine kernel, read by the mass and
+// pick kernels).
 enum : int32_t { kModeNone = 0, kModeBonus = 1, kModeResidual = 2 };
 struct alignas(16) ReqState {
   int32_t mode;
@@ -38,7 +36,6 @@ struct alignas(16) ReqState {
   float kscale;       // log2(e) / T, rounded to float
   float mt, md;       // row maxima
   float inv_st, inv_sd;  // 1 / row sums (float)
-  int32_t rec_row_t;  // record row index (request-major) of the target row a
   float st;           // target row a's sum
   float u;            // u' for the draw
   int32_t flags;
@@ -69,7 +66,7 @@ struct VerifyParams {
   uint8_t* out_flags;       // [B] nullable
   // workspace
   uint32_t* status;
-  uint32_t* cnt_sample;     // [B] per-request counter of the draw's chunk CTAs
+  ReqState* req;            // [B] draw state per request
   ChunkRecord* rec;         // [B * rows_per_req * nchunks]
   float* mass;              // [B * nchunks] residual mass per chunk
   float* mass_p;            // [B * nchunks] target-row weight per chunk (bonus draw / fallback)
@@ -96,7 +93,7 @@ struct ScheduleParams {
 
 // Workspace layout for SV_OP_VERIFY.
 struct VerifyLayout {
-  size_t status, cnt_sample, rec, mass, mass_p, total;
+  size_t status, req, rec, mass, mass_p, total;
 };
 VerifyLayout verify_layout(int B, int Kmax, int nchunks);
 void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);

@@ -531,35 +531,41 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 }
 
 // ------------------------------------------------------------------------------------------
-// finalize kernel: grid (nchunks, B) for sampled calls, (1, B) for greedy calls
+// combine (grid B), mass (grid (nchunks, B)) and pick (grid B) kernels, chained behind row_stats
+// with programmatic dependent launch
 // ------------------------------------------------------------------------------------------
 // Per-row statistics in shared memory (one entry per record row of the request).
 struct RowStatS {
-  float s;     // sum of 2^((x - m) k) over the row (merged over chunks in double)
+  float s;     // sum of 2^((x - m) k) over the row
   float m;     // row max
   int32_t g;   // first argmax (greedy rows)
   float xval;  // logit at the row's drafted token (sampled rows)
 };
 
-constexpr size_t kFinMaxStagedBytes = 48 * 1024;
-constexpr int kMaxRange = 1024;  // longest warp range: a 16 KB chunk of bf16 split eight ways  // records staged in shared memory up to this size
+constexpr size_t kFinMaxStagedBytes = 48 * 1024;  // chunk records staged in shared memory up to this
 constexpr int kFinMaxDynSmem = 96 * 1024;
+constexpr int kCombineThreads = 256, kCombineWarps = kCombineThreads / 32;
+constexpr int kMassThreads = 128, kMassWarps = kMassThreads / 32;
+constexpr int kPickThreads = 256, kPickWarps = kPickThreads / 32;
+constexpr int kPickStagedChunks = 2048;  // chunk masses staged in shared memory up to this many
 
-struct FinSmem {
-  ReqState st;      // what the draw needs (identical in every CTA of the request)
+struct CombineSmem {
   int a_min;
   uint32_t acc_flags;
   uint32_t bad;
-  float wsum[kSampleWarps];
-  float wsum_p[kSampleWarps];
-  int last;
+};
+
+struct PickSmem {
+  ReqState st;
+  float wsum[kPickWarps];
   int chunk;        // crossing chunk
   int bonus;        // draw from the target row (bonus, or residual mass 0)
   uint32_t flags;
   float base;       // mass before the crossing chunk
   float thr;        // u' * Z
-  int pick_thread;   // first thread whose entries hold the crossing
-  int last_pos;      // broadcast of the pick
+  int pick_thread;  // first thread whose entries hold the crossing
+  int last_pos;     // broadcast of the pick
+  float mass[2 * kPickStagedChunks];
 };
 
 // weight of vocabulary entry v of a row pair for the draw (target-only when !residual)
@@ -571,16 +577,17 @@ __device__ __forceinline__ float draw_weight(const char* trow, const char* drow,
   return fmaxf(0.0f, pv * st.inv_st - ex2_approx((load_logit<DT>(drow, v) - st.md) * st.kscale) * st.inv_sd);
 }
 
-// The eight warp ranges of a chunk: contiguous, warp w covers [lo, hi).
-__device__ __forceinline__ void warp_range(int len, int w, int* lo, int* hi) {
-  const int seg = (len + kSampleWarps - 1) / kSampleWarps;
+// Contiguous ranges of a chunk, one per warp: warp w of nw covers [lo, hi).
+__device__ __forceinline__ void warp_range(int len, int nw, int w, int* lo, int* hi) {
+  const int seg = (len + nw - 1) / nw;
   *lo = min(len, w * seg);
   *hi = min(len, *lo + seg);
 }
 
-// Sum of draw weights over [c0 + lo, c0 + hi) by one warp.  A warp range holds at most 128
-// 16-byte vectors, so each lane issues all of its loads (<= 4 per row) before using any.
-constexpr int kRangeVecPerLane = 4;
+// Sums over [c0 + lo, c0 + hi) by one warp: *sum_r of the residual max(0, p - q) (residual only)
+// and *sum_p of the target weights.  Vectors are loaded in batches of kBatch per lane, every
+// load of a batch issued before any is used.
+constexpr int kBatch = 4;
 template <int DT>
 __device__ void warp_range_sum(const char* trow, const char* drow, int c0, int lo, int hi, bool residual,
                                const ReqState& st, int lane, float* sum_r, float* sum_p) {
@@ -595,41 +602,41 @@ __device__ void warp_range_sum(const char* trow, const char* drow, int c0, int l
   const int len = hi - lo;
   const ChunkSplit a = split_chunk<kElt>(trow, c0 + lo, len);
   const ChunkSplit b = residual ? split_chunk<kElt>(drow, c0 + lo, len) : a;
-  if (a.nvec > 0 && a.head == b.head && a.nvec <= 32 * kRangeVecPerLane) {
+  if (a.nvec > 0 && a.head == b.head) {
     const int v0 = c0 + lo + a.head;
     const uint4* tv = reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(v0) * kElt);
     const uint4* dv = reinterpret_cast<const uint4*>(drow + static_cast<int64_t>(v0) * kElt);
-    uint4 tw[kRangeVecPerLane], dw[kRangeVecPerLane];
-#pragma unroll
-    for (int u = 0; u < kRangeVecPerLane; ++u) {
-      const int v = lane + 32 * u;
-      tw[u] = v < a.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
-      dw[u] = (residual && v < a.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
-    }
     const bool hh = lane < a.head, ht = lane < a.tail;
-    const float hx = hh ? load_logit<DT>(trow, c0 + lo + lane) : 0.0f;
-    const float hd = (hh && residual) ? load_logit<DT>(drow, c0 + lo + lane) : 0.0f;
-    const float tx_ = ht ? load_logit<DT>(trow, v0 + a.nvec * kVec + lane) : 0.0f;
-    const float td_ = (ht && residual) ? load_logit<DT>(drow, v0 + a.nvec * kVec + lane) : 0.0f;
+    if (hh) add(load_logit<DT>(trow, c0 + lo + lane), residual ? load_logit<DT>(drow, c0 + lo + lane) : 0.0f);
+    if (ht)
+      add(load_logit<DT>(trow, v0 + a.nvec * kVec + lane),
+          residual ? load_logit<DT>(drow, v0 + a.nvec * kVec + lane) : 0.0f);
+    for (int base = 0; base < a.nvec; base += 32 * kBatch) {
+      uint4 tw[kBatch], dw[kBatch];
 #pragma unroll
-    for (int u = 0; u < kRangeVecPerLane; ++u) {
-      if (lane + 32 * u >= a.nvec) break;
-      if constexpr (DT == SV_BF16) {
-        const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
+      for (int u = 0; u < kBatch; ++u) {
+        const int v = base + lane + 32 * u;
+        tw[u] = v < a.nvec ? __ldg(tv + v) : make_uint4(0, 0, 0, 0);
+        dw[u] = (residual && v < a.nvec) ? __ldg(dv + v) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          add(bf16_lo(t4[e]), bf16_lo(d4[e]));
-          add(bf16_hi(t4[e]), bf16_hi(d4[e]));
+      for (int u = 0; u < kBatch; ++u) {
+        if (base + lane + 32 * u >= a.nvec) break;
+        if constexpr (DT == SV_BF16) {
+          const uint32_t t4[4] = {tw[u].x, tw[u].y, tw[u].z, tw[u].w}, d4[4] = {dw[u].x, dw[u].y, dw[u].z, dw[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            add(bf16_lo(t4[e]), bf16_lo(d4[e]));
+            add(bf16_hi(t4[e]), bf16_hi(d4[e]));
+          }
+        } else {
+          add(__uint_as_float(tw[u].x), __uint_as_float(dw[u].x));
+          add(__uint_as_float(tw[u].y), __uint_as_float(dw[u].y));
+          add(__uint_as_float(tw[u].z), __uint_as_float(dw[u].z));
+          add(__uint_as_float(tw[u].w), __uint_as_float(dw[u].w));
         }
-      } else {
-        add(__uint_as_float(tw[u].x), __uint_as_float(dw[u].x));
-        add(__uint_as_float(tw[u].y), __uint_as_float(dw[u].y));
-        add(__uint_as_float(tw[u].z), __uint_as_float(dw[u].z));
-        add(__uint_as_float(tw[u].w), __uint_as_float(dw[u].w));
       }
     }
-    if (hh) add(hx, hd);
-    if (ht) add(tx_, td_);
   } else {
 #pragma unroll 4
     for (int e = lane; e < len; e += 32)
@@ -644,26 +651,27 @@ __device__ void warp_range_sum(const char* trow, const char* drow, int c0, int l
   *sum_p = acc_p;
 }
 
-// Inverse-CDF pick inside one chunk by the whole CTA.  Thread t owns the contiguous entries
-// [t*per, (t+1)*per) of the chunk (per <= 32), loaded with 16-byte vectors when the layout allows,
-// every load issued before any is used.  Returns the chunk-relative index of the first entry with
-// cumsum > rem, or, if rounding keeps every partial sum at or below rem, the last entry with
-// positive weight (-1 if none).  Called by all threads of the CTA.
+// Inverse-CDF pick inside one chunk by a whole kPickThreads CTA.  Thread t owns the contiguous
+// entries [t*per, (t+1)*per) of the chunk (per <= 32), loaded with 16-byte vectors when the layout
+// allows, every load issued before any is used.  Returns the chunk-relative index of the first
+// entry with cumsum > rem, or, if rounding keeps every partial sum at or below rem, the last entry
+// with positive weight (-1 if none).
 template <int DT>
 __device__ int block_pick(const char* trow, const char* drow, int c0, int len, bool residual, const ReqState& st,
-                          float rem, FinSmem* sm, int tid) {
+                          float rem, PickSmem* sm, int tid) {
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;
   constexpr int kMaxPer = 32;
   constexpr int kMaxV = 4;  // bf16: 32 entries, fp32: 16 entries per thread
   const int lane = tid & 31, warp = tid >> 5;
-  const int per = (len + kSampleThreads - 1) / kSampleThreads;
+  const int per = (len + kPickThreads - 1) / kPickThreads;
   const int a = min(len, tid * per), b = min(len, a + per);
   const int cnt = b - a;
   const char* tp = trow + static_cast<int64_t>(c0 + a) * kElt;
   const char* dp = drow + static_cast<int64_t>(c0 + a) * kElt;
   const bool vec = per % kVec == 0 && per / kVec <= kMaxV && cnt == per &&
-                   (reinterpret_cast<uintptr_t>(tp) & 15u) == 0 && (!residual || (reinterpret_cast<uintptr_t>(dp) & 15u) == 0);
+                   (reinterpret_cast<uintptr_t>(tp) & 15u) == 0 &&
+                   (!residual || (reinterpret_cast<uintptr_t>(dp) & 15u) == 0);
   float w[kMaxPer];
 #pragma unroll
   for (int j = 0; j < kMaxPer; ++j) w[j] = 0.0f;
@@ -700,11 +708,9 @@ __device__ int block_pick(const char* trow, const char* drow, int c0, int len, b
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
         const int j = u * kVec + e;
-        if (j < kMaxPer) {
+        if (j < kMaxPer && j < cnt) {
           const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
-          w[j] = (j < cnt) ? (residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd)
-                                       : pv)
-                           : 0.0f;
+          w[j] = residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
         }
       }
     }
@@ -720,7 +726,6 @@ __device__ int block_pick(const char* trow, const char* drow, int c0, int len, b
     sum += w[j];
     if (w[j] > 0.0f) lastpos = a + j;
   }
-  // block exclusive scan of the per-thread sums
   float incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -729,7 +734,7 @@ __device__ int block_pick(const char* trow, const char* drow, int c0, int len, b
   }
   if (lane == 31) sm->wsum[warp] = incl;
   if (tid == 0) {
-    sm->pick_thread = kSampleThreads;
+    sm->pick_thread = kPickThreads;
     sm->last_pos = -1;
   }
   __syncthreads();
@@ -787,7 +792,7 @@ __device__ int warp_find(int cnt, float thr, WF w, float* before, int lane) {
   return last_pos >= 0 ? last_pos : 0;
 }
 
-// Shared-memory plan of the finalize kernel: row statistics, then (when they fit) the request's
+// Shared-memory plan of the combine kernel: row statistics, then (when they fit) the request's
 // staged chunk records, then its drafted tokens.
 struct FinLayout {
   size_t rec_off, tok_off, bytes;
@@ -812,13 +817,14 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// ---- combine: one CTA per request --------------------------------------------------------
 template <int DT>
-__global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyParams p) {
   extern __shared__ __align__(16) unsigned char fin_dyn[];
-  __shared__ FinSmem sm;
+  __shared__ CombineSmem sm;
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.y, c = blockIdx.x;
+  const int i = blockIdx.x;
   const int NC = p.nchunks, R = p.rows_per_req, Kmax = p.Kmax;
   const FinLayout FL = fin_layout(R, NC, Kmax);
   RowStatS* rs = reinterpret_cast<RowStatS*>(fin_dyn);                        // [R]
@@ -827,12 +833,12 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   const ChunkRecord* rec_g = p.rec + static_cast<int64_t>(i) * R * NC;
   const int32_t* toks = p.tokens ? p.tokens + static_cast<int64_t>(i) * p.tok_stride : nullptr;
 
-  // ---------------- round 1: everything the combine reads, requested at once ----------------
-  // (records of all 2*Kmax+1 record rows and all Kmax tokens; entries past n are ignored)
+  // round 1: everything the combine reads, requested at once (records of all 2*Kmax+1 record
+  // rows and all Kmax tokens; entries past n are ignored)
   if (FL.staged)
-    for (int j = tid; j < R * NC; j += kSampleThreads) cp_async16(rec_s + j, rec_g + j);
+    for (int j = tid; j < R * NC; j += kCombineThreads) cp_async16(rec_s + j, rec_g + j);
   if (toks)
-    for (int j = tid; j < Kmax; j += kSampleThreads) cp_async4(tok_s + j, toks + j);
+    for (int j = tid; j < Kmax; j += kCombineThreads) cp_async4(tok_s + j, toks + j);
   uint32_t bad_in;
   const uint16_t info = request_info(p, i, &bad_in);
   const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
@@ -840,15 +846,15 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   cp_async_wait_all();
   __syncthreads();
   if (info & kInfoInvalid) {
-    if (c == 0) {
-      if (tid == 0) atomicOr(p.status, bad_in);
-      write_invalid(p, i, tid, kSampleThreads);
+    if (tid == 0) {
+      atomicOr(p.status, bad_in);
+      p.req[i].mode = kModeNone;
     }
+    write_invalid(p, i, tid, kCombineThreads);
     return;
   }
   const int n = info & kInfoN;
   const bool sampled = info & kInfoSampled;
-  if (!sampled && c > 0) return;
   const bool need_draft = info & kInfoNeedDraft;
   const float kscale = sampled ? kscale_of(T) : 0.0f;
   const int nrows = n + 1 + (need_draft ? n : 0);
@@ -856,7 +862,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   auto tok = [&](int k) { return toks ? tok_s[k] : rs[Kmax + 1 + k].g; };
 
   // 1. row statistics: one warp per row, one pass over the row's chunk records
-  for (int q = warp; q < nrows; q += kSampleWarps) {
+  for (int q = warp; q < nrows; q += kCombineWarps) {
     const bool is_target = q <= n;
     const int k = is_target ? q : q - n - 1;
     const int r = is_target ? k : Kmax + 1 + k;
@@ -866,7 +872,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
     float m = -INFINITY, xval = NAN, S = 0.0f;
     int g = -1;
     if (sampled) {
-      // row max, then the chunk sums rescaled to it, added with a compensated (TwoSum) tree
+      // row max, then the piece sums rescaled to it, added with a compensated (TwoSum) tree
       for (int cc = lane; cc < NC; cc += 32) {
         const ChunkRecord rc = FL.staged ? rr[cc] : ld_record(rr + cc);
         m = fmaxf(m, rc.m);
@@ -916,7 +922,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   __syncthreads();
 
   // 2. accept tests (each position independently; the first rejection is a min-reduction)
-  for (int k = tid; k < n; k += kSampleThreads) {
+  for (int k = tid; k < n; k += kCombineThreads) {
     const int x = tok(k);
     bool acc;
     float pv, qv;
@@ -936,113 +942,125 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
       acc = u * qv < pv;
       if (qv == 0.0f) atomicOr(&sm.acc_flags, SV_FLAG_Q_ZERO);
     }
-    if (c == 0 && p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = pv;
-    if (c == 0 && p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = qv;
+    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = pv;
+    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = qv;
     if (!acc) atomicMin(&sm.a_min, k);
   }
-  if (c == 0) {
-    for (int k = n + tid; k < Kmax; k += kSampleThreads) {
-      if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
-      if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
-    }
+  for (int k = n + tid; k < Kmax; k += kCombineThreads) {
+    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
+    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
   }
   __syncthreads();
   if (sm.bad) {
-    if (c == 0) {
-      if (tid == 0) atomicOr(p.status, sm.bad);
-      write_invalid(p, i, tid, kSampleThreads);
+    if (tid == 0) {
+      atomicOr(p.status, sm.bad);
+      p.req[i].mode = kModeNone;
     }
+    write_invalid(p, i, tid, kCombineThreads);
     return;
   }
   const int a = sm.a_min;
 
   // 3. emit: the accepted prefix (and, greedy, the target argmax at a); a sampled request's
-  //    token at a is written by the CTA that draws it
-  if (c == 0) {
-    for (int j = tid; j <= Kmax; j += kSampleThreads) {
-      if (j == a && sampled) continue;
-      int v = -1;
-      if (j < a) v = tok(j);
-      else if (j == a) v = rs[a].g;
-      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
-    }
-    if (tid == 0) {
-      p.out_accept_len[i] = a;
-      if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(sm.acc_flags);
-    }
+  //    token at a is written by the pick kernel
+  for (int j = tid; j <= Kmax; j += kCombineThreads) {
+    if (j == a && sampled) continue;
+    int v = -1;
+    if (j < a) v = tok(j);
+    else if (j == a) v = rs[a].g;
+    p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
   }
-  if (!sampled) return;
-  const int mode = a < n ? kModeResidual : kModeBonus;
   if (tid == 0) {
+    p.out_accept_len[i] = a;
+    if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(sm.acc_flags);
     ReqState st = {};
-    st.mode = mode;
-    st.a = a;
-    st.flags = static_cast<int32_t>(sm.acc_flags);
-    st.row_t = target_row(p, i, a);
-    st.kscale = kscale;
-    st.mt = rs[a].m;
-    st.st = rs[a].s;
-    st.inv_st = __frcp_rn(rs[a].s);
-    if (mode == kModeResidual) {
-      st.row_d = draft_row(p, i, a);
-      st.md = rs[Kmax + 1 + a].m;
-      st.inv_sd = __frcp_rn(rs[Kmax + 1 + a].s);
+    st.mode = kModeNone;
+    if (sampled) {
+      st.mode = a < n ? kModeResidual : kModeBonus;
+      st.a = a;
+      st.flags = static_cast<int32_t>(sm.acc_flags);
+      st.row_t = target_row(p, i, a);
+      st.kscale = kscale;
+      st.mt = rs[a].m;
+      st.st = rs[a].s;
+      st.inv_st = __frcp_rn(rs[a].s);
+      if (a < n) {
+        st.row_d = draft_row(p, i, a);
+        st.md = rs[Kmax + 1 + a].m;
+        st.inv_sd = __frcp_rn(rs[Kmax + 1 + a].s);
+      }
+      st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
     }
-    st.rec_row_t = a;  // record row inside the request
-    st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
-    sm.st = st;
+    p.req[i] = st;
+  }
+}
+
+// ---- mass: one light CTA per (request, chunk) --------------------------------------------
+// Chunk sums of the residual max(0, p_a - q_a) after a rejection, and of the target weights
+// of row a (the bonus draw, or the fallback when the residual mass is zero).
+template <int DT>
+__global__ void __launch_bounds__(kMassThreads) mass_kernel(const VerifyParams p) {
+  __shared__ ReqState st;
+  __shared__ float wr_s[kMassWarps], wp_s[kMassWarps];
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.y, c = blockIdx.x, NC = p.nchunks;
+  if (tid == 0) st = p.req[i];
+  __syncthreads();
+  if (st.mode == kModeNone) return;
+  const bool residual = st.mode == kModeResidual;
+  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
+  const char* drow = residual ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
+  const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+  int lo, hi;
+  warp_range(len, kMassWarps, warp, &lo, &hi);
+  float wr, wp;
+  warp_range_sum<DT>(trow, drow, c0, lo, hi, residual, st, lane, &wr, &wp);
+  if (lane == 0) {
+    wr_s[warp] = wr;
+    wp_s[warp] = wp;
   }
   __syncthreads();
+  if (tid == 0) {
+    float tr = 0.0f, tp = 0.0f;
+    for (int w = 0; w < kMassWarps; ++w) {
+      tr += wr_s[w];
+      tp += wp_s[w];
+    }
+    p.mass[static_cast<int64_t>(i) * NC + c] = tr;
+    p.mass_p[static_cast<int64_t>(i) * NC + c] = tp;
+  }
+}
 
-  // ---------------- draw at position a ----------------
-  // Every CTA of the request sums its chunk: the residual max(0, p_a - q_a) after a rejection,
-  // and the target weights of row a (the bonus draw, or the fallback when the residual mass is
-  // zero).  The request's last CTA then finds the crossing chunk and entry.
+// ---- pick: one CTA per request -------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p) {
+  __shared__ PickSmem sm;
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, NC = p.nchunks, Kmax = p.Kmax;
+  if (tid == 0) sm.st = p.req[i];
+  __syncthreads();
   const ReqState& st = sm.st;
+  if (st.mode == kModeNone) return;
   const bool residual_mode = st.mode == kModeResidual;
   const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
   const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
-  float* mass_s = reinterpret_cast<float*>(fin_dyn + FL.rec_off);  // reuses the staged records' space
-  const bool stage_mass = FL.staged && static_cast<size_t>(NC) * 8 <= static_cast<size_t>(R) * NC * sizeof(ChunkRecord);
-  float* mass_r = p.mass + static_cast<int64_t>(i) * NC;
-  float* mass_p = p.mass_p + static_cast<int64_t>(i) * NC;
-  {
-    const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
-    int lo, hi;
-    warp_range(len, warp, &lo, &hi);
-    float wr, wp;
-    warp_range_sum<DT>(trow, drow, c0, lo, hi, residual_mode, st, lane, &wr, &wp);
-    if (lane == 0) {
-      sm.wsum[warp] = wr;
-      sm.wsum_p[warp] = wp;
+  const float* mass_r = p.mass + static_cast<int64_t>(i) * NC;
+  const float* mass_p = p.mass_p + static_cast<int64_t>(i) * NC;
+  const bool staged = NC <= kPickStagedChunks;
+  if (staged) {  // one round for every chunk mass of the request
+    for (int j = tid; j < NC; j += kPickThreads) {
+      sm.mass[j] = mass_r[j];
+      sm.mass[kPickStagedChunks + j] = mass_p[j];
     }
-    __syncthreads();
-    if (tid == 0) {
-      float tr = 0.0f, tp = 0.0f;
-      for (int w = 0; w < kSampleWarps; ++w) {
-        tr += sm.wsum[w];
-        tp += sm.wsum_p[w];
-      }
-      __stcg(mass_r + c, tr);
-      __stcg(mass_p + c, tp);
-      const uint32_t old = atom_add_acq_rel(p.cnt_sample + i, 1u);  // release: the masses above
-      sm.last = (old + 1u == static_cast<uint32_t>(NC)) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!sm.last) return;
-    if (tid == 0) p.cnt_sample[i] = 0;
-    if (stage_mass)  // one round for every chunk mass of the request
-      for (int j = tid; j < NC; j += kSampleThreads) {
-        mass_s[j] = __ldcg(mass_r + j);
-        mass_s[NC + j] = __ldcg(mass_p + j);
-      }
-    __syncthreads();
   }
+  __syncthreads();
 
-  // one CTA per request from here on: find the crossing chunk
+  // the crossing chunk (one warp)
   if (warp == 0) {
-    auto r_at = [&](int cc) { return stage_mass ? mass_s[cc] : __ldcg(mass_r + cc); };
-    auto p_at = [&](int cc) { return stage_mass ? mass_s[NC + cc] : __ldcg(mass_p + cc); };
+    auto r_at = [&](int cc) { return staged ? sm.mass[cc] : mass_r[cc]; };
+    auto p_at = [&](int cc) { return staged ? sm.mass[kPickStagedChunks + cc] : mass_p[cc]; };
     int bonus = residual_mode ? 0 : 1;
     uint32_t flags = 0;
     float Z = 0.0f;
@@ -1076,10 +1094,7 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
   const int cstar = sm.chunk;
   const bool residual = !sm.bonus;
   const int c0 = cstar * p.chunk_len, len = min(p.chunk_len, p.V - c0);
-  const char* dr = residual ? drow : trow;
-
-  // the crossing entry inside the chunk (the whole CTA)
-  int y = block_pick<DT>(trow, dr, c0, len, residual, st, sm.thr - sm.base, &sm, tid);
+  int y = block_pick<DT>(trow, residual ? drow : trow, c0, len, residual, st, sm.thr - sm.base, &sm, tid);
   if (tid == 0) {
     if (y < 0) y = 0;  // only if every weight of the chunk flushed to zero; keep a valid token
     p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + y;
@@ -1090,6 +1105,29 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const VerifyPa
 bool g_stats_attr_set[2] = {false, false};
 bool g_fin_attr_set[2] = {false, false};
 int g_num_sms = 0;
+
+// Launch `kernel` behind the previous kernel on the stream with programmatic dependent launch
+// (its launch overlaps the previous grid's tail; it waits in griddepcontrol.wait).  Left out
+// while instrumentation puts events between kernels.
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t stream, int prof_id,
+                       const VerifyParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = prof_enabled() ? 0 : 1;
+  prof_before(prof_id, stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+  prof_after(prof_id, stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 template <int DT>
 cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
@@ -1122,28 +1160,20 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (!g_fin_attr_set[di]) {
-    if ((e = cudaFuncSetAttribute(finalize_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(combine_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kFinMaxDynSmem)) != cudaSuccess)
       return e;
     g_fin_attr_set[di] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(sampled ? p.nchunks : 1), static_cast<unsigned>(p.B), 1);
-  cfg.blockDim = dim3(kSampleThreads, 1, 1);
-  cfg.dynamicSmemBytes = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  // Programmatic dependent launch lets the finalize grid's launch overlap the row_stats tail;
-  // it is left out while instrumentation puts an event between the two kernels.
-  cfg.numAttrs = prof_enabled() ? 0 : 1;
-  prof_before(SV_KERNEL_FINALIZE, stream);
-  e = cudaLaunchKernelEx(&cfg, finalize_kernel<DT>, p);
-  prof_after(SV_KERNEL_FINALIZE, stream);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  const size_t csmem = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
+  if ((e = launch_pdl(combine_kernel<DT>, dim3(p.B), kCombineThreads, csmem, stream, SV_KERNEL_COMBINE, p)) !=
+      cudaSuccess)
+    return e;
+  if (!sampled) return cudaSuccess;
+  if ((e = launch_pdl(mass_kernel<DT>, dim3(p.nchunks, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p)) !=
+      cudaSuccess)
+    return e;
+  return launch_pdl(pick_kernel<DT>, dim3(p.B), kPickThreads, 0, stream, SV_KERNEL_PICK, p);
 }
 
 }  // namespace
@@ -1169,8 +1199,8 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   size_t off = 0;
   L.status = off;
   off = align256(off + 256);
-  L.cnt_sample = off;
-  off = align256(off + sizeof(uint32_t) * B);
+  L.req = off;
+  off = align256(off + sizeof(ReqState) * B);
   L.mass = off;
   off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
   L.mass_p = off;
