@@ -52,6 +52,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Pairs of floats in one 64-bit register for the packed f32x2 arithmetic of sm_100 and later:
+// one instruction performs two independently rounded float operations.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// (2^(x.lo k - c), 2^(x.hi k - c)) with k2 = (k, k) and nc2 = (-c, -c).
+__device__ __forceinline__ f32x2 f2_exp2_offset(f32x2 x, f32x2 k2, f32x2 nc2) {
+  float d0, d1;
+  f2_unpack(f2_fma(x, k2, nc2), d0, d1);
+  return f2_pack(ex2_approx(d0), ex2_approx(d1));
+}
+
 template <int DT>
 __device__ __forceinline__ float load_logit(const void* row, int64_t v) {
   if constexpr (DT == SV_BF16) {
@@ -62,7 +90,19 @@ __device__ __forceinline__ float load_logit(const void* row, int64_t v) {
   }
 }
 
-// Merge two (max, sum of 2^((x - max) * k)) pairs.  A max of -inf means an empty sum.
+// Exponent offset of a sampled row piece whose largest logit is m: c(m) = rint(m k), an
+// integer-valued float.  A piece stores (m, s) with s = sum of 2^(x k - c(m)) over its logits:
+// each term is one fused multiply-add and one ex2, every term is at most 2^0.5, and two pieces'
+// sums rescale to a common offset by exact powers of two.
+__device__ __forceinline__ float exp_offset(float m, float k) { return rintf(__fmul_rn(m, k)); }
+
+// 2^d for an integer-valued d <= 0 (0 below the normal float range).
+__device__ __forceinline__ float pow2_nonpos(float d) {
+  const int e = static_cast<int>(fmaxf(d, -127.0f));
+  return e <= -127 ? 0.0f : __int_as_float((e + 127) << 23);
+}
+
+// Merge two (max, sum of 2^(x k - c(max))) pairs.  A max of -inf means an empty sum.
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float k) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
@@ -71,7 +111,8 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
     return;
   }
   const float M = fmaxf(m, m2);
-  s = s * ex2_approx((m - M) * k) + s2 * ex2_approx((m2 - M) * k);
+  const float C = exp_offset(M, k);
+  s = s * pow2_nonpos(exp_offset(m, k) - C) + s2 * pow2_nonpos(exp_offset(m2, k) - C);
   m = M;
 }
 

@@ -20,7 +20,7 @@ static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split
 // Per-(row, chunk) statistics written by row_stats.
 struct alignas(16) ChunkRecord {
   float m;     // max logit in the chunk
-  float s;     // sum of 2^((x - m) * log2(e) / T) over the chunk (0 for greedy rows)
+  float s;     // sum of 2^(x k - rint(m k)) over the chunk, k = log2(e) / T (0 for greedy rows)
   int32_t g;   // first argmax in the chunk (vocabulary index), greedy rows only
   float xval;  // logit at the row's drafted token, when that token lies in the chunk
 };
@@ -34,7 +34,7 @@ struct alignas(16) ReqState {
   int64_t row_t;      // absolute target row index of row a
   int64_t row_d;      // absolute draft row index of row a (residual mode)
   float kscale;       // log2(e) / T, rounded to float
-  float mt, md;       // row maxima
+  float ct, cd;       // exponent offsets exp_offset(row max, kscale) of the two rows
   float inv_st, inv_sd;  // 1 / row sums (float)
   float st;           // target row a's sum
   float u;            // u' for the draw

@@ -9,7 +9,8 @@
 //   U(K) = sum of round(s * 2^48) over the kept slots (exact int64, order independent)
 //   pick the K maximising U / c(K) (or U - c(K)), c(K) = a + b K; ties -> smaller K
 // The ranking is a bitonic sort of 64-bit keys (~bits(s) : request : position) in shared
-// memory; with s >= 0 the float bits order like unsigned integers.
+// memory; with s >= 0 the float bits order like unsigned integers.  U(K) for every candidate
+// comes from one integer prefix scan of the sorted order.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -68,10 +69,6 @@ __device__ int block_exclusive_scan(int v, int* excl, int* warp_tot) {
   const int total = warp_tot[32];
   __syncthreads();
   return total;
-}
-
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
 // Bitonic merge step for one element: keep the smaller key when this element is the lower index
@@ -134,69 +131,159 @@ __device__ void bitonic_sort(unsigned long long* keys, int P) {
   __syncthreads();
 }
 
+// Inclusive scan, across the CTA, of E 64-bit values per thread: thread t's value e belongs to
+// row e at column t (element e * kSchedThreads + t of the sorted order).  On return v[e] holds
+// the inclusive prefix within its row and row_tot[e] row e's total.
+template <int E>
+__device__ void block_row_scan64(long long (&v)[E], long long* wtot, long long* row_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xFFFFFFFFu, v[e], o);
+      if (lane >= o) v[e] += y;
+    }
+    if (lane == 31) wtot[e * 32 + warp] = v[e];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int e = 0; e < E; ++e) {
+      const long long w = wtot[e * 32 + lane];
+      long long wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      wtot[e * 32 + lane] = wi - w;  // exclusive prefix of the warp totals
+      if (lane == 31) row_tot[e] = wi;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] += wtot[e * 32 + warp];
+}
+
+struct SchedSmem {
+  long long wtot[16 * 32];
+  long long row_tot[16];
+  long long ucand[8];
+  double obj[8];
+  int cand[8];
+  int ncand;
+  int warp_tot[33];
+  unsigned int bad;
+};
+
+// Sort, then U(K) of every candidate, the objective, and the chosen K (same in every thread).
+template <int E>
+__device__ void sort_and_choose(const ScheduleParams& p, unsigned long long* keys, int P, int B, SchedSmem& sm,
+                                int* Kb, long long* Ub) {
+  const int tid = threadIdx.x;
+  // ascending key == (s desc, request asc, position asc)
+  bitonic_sort<E>(keys, P);
+  const int nc = sm.ncand;  // written by thread 0 before the sort's barriers
+
+  // U(K) = sum of round(s * 2^48) over the first K - B sorted slots: one scan of the sorted
+  // order, read at each candidate (exact integer sums)
+  long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = q48_of_key(keys[e * kSchedThreads + tid]);  // padding gives 0
+  block_row_scan64<E>(v, sm.wtot, sm.row_tot);
+  for (int c = 0; c < nc; ++c) {
+    const int L = sm.cand[c] - B;  // slots beyond the always-kept roots
+    if (L == 0) {
+      if (tid == 0) sm.ucand[c] = 0;
+    } else if (((L - 1) & (kSchedThreads - 1)) == tid) {
+      const int er = (L - 1) / kSchedThreads;
+      long long u = 0;
+      for (int e = 0; e < er; ++e) u += sm.row_tot[e];
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (e == er) u += v[e];
+      sm.ucand[c] = u;
+    }
+  }
+  __syncthreads();
+
+  // objective (float64 with explicit rounding: no contraction), one thread per candidate
+  if (tid < nc) {
+    const long long U = sm.ucand[tid] + static_cast<long long>(B) * (1ll << 48);
+    const double util = __dmul_rn(__ll2double_rn(U), kTwoM48);
+    const double cost = __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(sm.cand[tid])));
+    sm.obj[tid] = p.objective == SV_OBJ_NET ? __dsub_rn(util, cost) : __ddiv_rn(util, cost);
+    sm.ucand[tid] = U;
+  }
+  __syncthreads();
+  int bc = 0;  // ties -> the smaller K (candidates are ascending)
+  for (int c = 1; c < nc; ++c)
+    if (sm.obj[c] > sm.obj[bc]) bc = c;
+  *Kb = sm.cand[bc];
+  *Ub = sm.ucand[bc];
+}
+
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int B = p.B, Dmax = p.Dmax, P = p.sort_size;
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);                  // [P]
-  float* alpha_s = reinterpret_cast<float*>(smem + static_cast<size_t>(P) * 8);             // [B * Dmax]
-  int* cnt = reinterpret_cast<int*>(smem + static_cast<size_t>(P) * 8 +
-                                    ((static_cast<size_t>(B) * Dmax * 4 + 15) & ~size_t(15)));  // [B]
-  __shared__ int warp_tot[33];
-  __shared__ unsigned int bad;
-  __shared__ long long usum[8];
-  __shared__ int cand[8];
-  __shared__ int ncand;
-  __shared__ int bestK;
-  __shared__ long long bestU;
+  // keys [P]; kept flags [Dmax][B], position-major: request i's position k at (k - 1) * B + i
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+  uint8_t* kept = smem + static_cast<size_t>(P) * 8;
+  __shared__ SchedSmem sm;
 
-  const int tid = threadIdx.x;
-  if (tid == 0) bad = 0;
-  if (tid < 8) usum[tid] = 0;
-
-  // 0. one round of asynchronous copies: every confidence and every draft length
-  for (int j = tid; j < B * Dmax; j += kSchedThreads) {
-    const int i = j / Dmax, k = j - (j / Dmax) * Dmax;
-    cp_async4(alpha_s + j, p.alpha + static_cast<int64_t>(i) * p.alpha_stride + k);
-  }
-  if (p.draft_len)
-    for (int i = tid; i < B; i += kSchedThreads) cp_async4(cnt + i, p.draft_len + i);
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) sm.bad = 0;
   __syncthreads();
 
-  // 1. per-request lengths and their exclusive scan (each thread owns a contiguous block)
+  // 0. each thread owns a contiguous block of requests: their lengths and confidences (all Dmax
+  //    confidences of a request are requested together; entries past D_i are not used), the
+  //    prefix products (float32, left to right) and the sort keys (~bits(s) : request :
+  //    position) of their non-root slots, stored position-major so that neighbouring threads
+  //    write neighbouring words.  Slots past D_i get the largest key (sorted last, never kept).
   const int per = (B + kSchedThreads - 1) / kSchedThreads;
   const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
   int local = 0;
   for (int i = r0; i < r1; ++i) {
-    const int D = p.draft_len ? cnt[i] : Dmax;
-    if (D < 0 || D > Dmax) atomicOr(&bad, SV_DEV_BAD_DRAFT_LEN);
+    const int D = p.draft_len ? __ldg(p.draft_len + i) : Dmax;
+    if (D < 0 || D > Dmax) atomicOr(&sm.bad, SV_DEV_BAD_DRAFT_LEN);
     const int Dc = min(max(D, 0), Dmax);
-    cnt[i] = Dc;
+    const float* a_row = p.alpha + static_cast<int64_t>(i) * p.alpha_stride;
+    float s = 1.0f;
+    for (int k0 = 0; k0 < Dmax; k0 += 8) {
+      float a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = k0 + u < Dmax ? __ldg(a_row + k0 + u) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u + 1;
+        if (k > Dmax) break;
+        unsigned long long key = ~0ull;
+        if (k <= Dc) {
+          if (!(a[u] >= 0.0f && a[u] <= 1.0f)) atomicOr(&sm.bad, SV_DEV_BAD_ALPHA);
+          s = __fmul_rn(s, a[u]);
+          const uint32_t bits = __float_as_uint(s > 0.0f ? s : 0.0f);  // -0 sorts as +0
+          key = (static_cast<unsigned long long>(~bits) << 32) | (static_cast<unsigned long long>(i) << 10) |
+                static_cast<unsigned long long>(k);
+        }
+        keys[static_cast<int64_t>(k - 1) * B + i] = key;
+        kept[static_cast<int64_t>(k - 1) * B + i] = 0;
+      }
+    }
     local += Dc;
   }
-  int excl;
-  const int M = block_exclusive_scan(local, &excl, warp_tot);
-
-  // 2. prefix-confidence products and sort keys of the non-root slots
-  for (int i = r0, start = excl; i < r1; ++i) {
-    const int D = cnt[i];
-    float s = 1.0f;
-    for (int k = 1; k <= D; ++k) {
-      const float a = alpha_s[i * Dmax + (k - 1)];
-      if (!(a >= 0.0f && a <= 1.0f)) atomicOr(&bad, SV_DEV_BAD_ALPHA);
-      s = __fmul_rn(s, a);
-      const uint32_t bits = __float_as_uint(s > 0.0f ? s : 0.0f);  // -0 sorts as +0
-      keys[start + k - 1] = (static_cast<unsigned long long>(~bits) << 32) |
-                            (static_cast<unsigned long long>(i) << 10) | static_cast<unsigned long long>(k);
-    }
-    start += D;
-  }
-  for (int j = M + tid; j < P; j += kSchedThreads) keys[j] = ~0ull;
+  for (int j = B * Dmax + tid; j < P; j += kSchedThreads) keys[j] = ~0ull;
+  int wsum = local;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+  if (lane == 0) sm.warp_tot[warp] = wsum;
   __syncthreads();
+  int M = 0;  // non-root slots of the batch
+#pragma unroll
+  for (int w = 0; w < kSchedThreads / 32; ++w) M += sm.warp_tot[w];
 
-  if (bad) {
+  if (sm.bad) {
     if (tid == 0) {
-      atomicOr(p.status, bad);
+      atomicOr(p.status, sm.bad);
       *p.out_total_K = -1;
       if (p.out_utility_q48) *p.out_utility_q48 = -1;
     }
@@ -206,113 +293,70 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
     return;
   }
 
-  // 3. bitonic sort, ascending key == (s desc, request asc, position asc)
-  switch (P / kSchedThreads) {
-    case 1: bitonic_sort<1>(keys, P); break;
-    case 2: bitonic_sort<2>(keys, P); break;
-    case 4: bitonic_sort<4>(keys, P); break;
-    case 8: bitonic_sort<8>(keys, P); break;
-    default: bitonic_sort<16>(keys, P); break;
-  }
-
-  // 4. candidate budgets (eq. K_rho), clipped to [B, cap]: one thread per ratio
+  // 1. candidate budgets (eq. K_rho) clipped to [B, cap], ascending, duplicates dropped.  Thread
+  //    0 computes them while the other threads start the sort; the sort's barriers publish them.
   const int N = M + B;
-  if (tid < 8) {
-    int K = -1;
-    if (tid < p.n_ratios) {
-      const int cap = p.budget > 0 ? min(p.budget, N) : N;
-      K = static_cast<int>(ceil(static_cast<double>(p.ratios[tid]) * static_cast<double>(N)));
-      K = max(B, K);
+  if (tid == 0) {
+    const int cap = p.budget > 0 ? min(p.budget, N) : N;
+    int nc = 0;
+    for (int r = 0; r < p.n_ratios; ++r) {
+      int K = static_cast<int>(ceil(static_cast<double>(p.ratios[r]) * static_cast<double>(N)));
+      K = max(K, B);
       K = min(K, cap);
       K = max(K, B);
-    }
-    cand[tid] = K;
-  }
-  __syncthreads();
-  if (tid == 0) {  // sort ascending, drop duplicates and unused slots
-    int nc = 0;
-    for (int a = 0; a < 8; ++a) {
-      const int K = cand[a];
-      if (K < 0) continue;
       bool dup = false;
-      for (int c = 0; c < nc; ++c) dup |= cand[c] == K;
+      for (int c = 0; c < nc; ++c) dup |= sm.cand[c] == K;
       if (dup) continue;
       int pos = nc++;
-      while (pos > 0 && cand[pos - 1] > K) {
-        cand[pos] = cand[pos - 1];
+      while (pos > 0 && sm.cand[pos - 1] > K) {
+        sm.cand[pos] = sm.cand[pos - 1];
         --pos;
       }
-      cand[pos] = K;
+      sm.cand[pos] = K;
     }
-    ncand = nc;
+    sm.ncand = nc;
   }
-  __syncthreads();
 
-  // 5. U(K) for every candidate: exact integer sums over the sorted prefix
-  long long part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const int nc = ncand;
-  int lim[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) lim[c] = c < nc ? cand[c] - B : 0;
-  for (int j = tid; j < M; j += kSchedThreads) {
-    const long long q = q48_of_key(keys[j]);
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      if (j < lim[c]) part[c] += q;
+  // 2-5. sort, utilities, objective, chosen K
+  int Kb = B;
+  long long Ub = 0;
+  switch (P / kSchedThreads) {
+    case 1: sort_and_choose<1>(p, keys, P, B, sm, &Kb, &Ub); break;
+    case 2: sort_and_choose<2>(p, keys, P, B, sm, &Kb, &Ub); break;
+    case 4: sort_and_choose<4>(p, keys, P, B, sm, &Kb, &Ub); break;
+    case 8: sort_and_choose<8>(p, keys, P, B, sm, &Kb, &Ub); break;
+    default: sort_and_choose<16>(p, keys, P, B, sm, &Kb, &Ub); break;
   }
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    if (c >= nc) break;
-    long long v = part[c];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if ((tid & 31) == 0 && v != 0) atomicAdd(reinterpret_cast<unsigned long long*>(&usum[c]),
-                                             static_cast<unsigned long long>(v));
-  }
-  __syncthreads();
 
-  // 6. objective (float64 with explicit rounding: no contraction), one thread per candidate;
-  //    ties -> smaller K
-  __shared__ double obj_s[8];
-  if (tid < nc) {
-    const long long U = usum[tid] + static_cast<long long>(B) * (1ll << 48);
-    const double util = __dmul_rn(__ll2double_rn(U), kTwoM48);
-    const double cost = __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(cand[tid])));
-    obj_s[tid] = p.objective == SV_OBJ_NET ? __dsub_rn(util, cost) : __ddiv_rn(util, cost);
-    usum[tid] = U;
+  // 6. kept slots: the first Kb - B sorted keys, marked at their (position, request) place; a
+  //    request's kept slots are a prefix of its positions, so its depth is their count
+  for (int j = tid; j < Kb - B; j += kSchedThreads) {
+    const unsigned long long key = keys[j];
+    const int i = static_cast<int>((key >> 10) & 0x3FFFFFull), k = static_cast<int>(key & 0x3FFull);
+    kept[static_cast<int64_t>(k - 1) * B + i] = 1;
   }
-  __syncthreads();
-  if (tid == 0) {
-    int bc = 0;
-    for (int c = 1; c < nc; ++c)
-      if (obj_s[c] > obj_s[bc]) bc = c;
-    bestK = cand[bc];
-    bestU = usum[bc];
-  }
-  for (int i = tid; i < B; i += kSchedThreads) cnt[i] = 0;
   __syncthreads();
 
   // 7. per-request kept depth and packed row offsets
-  const int Kb = bestK;
-  for (int j = tid; j < Kb - B; j += kSchedThreads) atomicAdd(&cnt[(keys[j] >> 10) & 0x3FFFFFull], 1);
-  __syncthreads();
   int loc = 0;
   for (int i = r0; i < r1; ++i) {
-    p.out_keep_len[i] = cnt[i];
-    loc += cnt[i] + 1;
+    int n = 0;
+    for (int k = 0; k < Dmax; ++k) n += kept[static_cast<int64_t>(k) * B + i];
+    p.out_keep_len[i] = n;
+    loc += n + 1;
   }
   int rexcl;
-  const int rtot = block_exclusive_scan(loc, &rexcl, warp_tot);
+  const int rtot = block_exclusive_scan(loc, &rexcl, sm.warp_tot);
   if (p.out_row_offsets) {
     for (int i = r0, o = rexcl; i < r1; ++i) {
       p.out_row_offsets[i] = o;
-      o += cnt[i] + 1;
+      o += p.out_keep_len[i] + 1;
     }
     if (tid == 0) p.out_row_offsets[B] = rtot;
   }
   if (tid == 0) {
     *p.out_total_K = Kb;
-    if (p.out_utility_q48) *p.out_utility_q48 = bestU;
+    if (p.out_utility_q48) *p.out_utility_q48 = Ub;
   }
 }
 
@@ -322,11 +366,11 @@ bool g_sched_attr_set = false;
 
 int launch_schedule(const ScheduleParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t dyn = static_cast<size_t>(p.sort_size) * 8 +
-                     ((static_cast<size_t>(p.B) * p.Dmax * 4 + 15) & ~size_t(15)) + static_cast<size_t>(p.B) * 4;
+  // sort keys, then one kept flag per slot
+  const size_t dyn = static_cast<size_t>(p.sort_size) * 8 + static_cast<size_t>(p.B) * p.Dmax;
   cudaError_t e;
   if (!g_sched_attr_set) {
-    const int max_dyn = SV_MAX_SCHEDULE_SLOTS * 8 + SV_MAX_SCHEDULE_SLOTS * 4 + SV_MAX_BATCH * 4;
+    const int max_dyn = SV_MAX_SCHEDULE_SLOTS * 8 + SV_MAX_SCHEDULE_SLOTS;
     if ((e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn)) !=
         cudaSuccess)
       return static_cast<int>(e);

@@ -1,27 +1,25 @@
 // Verification kernels of libsv.
 //
 // row_stats  One streaming pass over every logit row a round needs.  A persistent grid walks
-//            (request, row, vocabulary chunk) tasks in request-major order; per CTA one
-//            producer lane issues 1-D bulk copies (cp.async.bulk) of <= 16 KB chunks into a
-//            4-stage shared-memory ring and eight consumer warps reduce each chunk to a record
-//            {max, sum 2^((x-max) log2(e)/T), first argmax, logit at the drafted token}.  The
-//            kernel only streams and writes records: no atomics, no fences, no waiting on other
-//            CTAs.
-// finalize   Launched behind row_stats with programmatic dependent launch, grid (chunks, B).
-//            Every CTA of request i merges the request's records into row statistics in shared
-//            memory and runs the accept chain: the greedy test x_k == argmax, or the rejection
-//            test u_k q_k(x_k) < p_k(x_k), first rejection = accepted length (AngelSpec
-//            explainer, "MTP: fix position 2 and 3", eq. L_e2e: one rejection voids every later
-//            position; AngelSpec release article, "Why one universal drafter underperforms":
-//            rejection-sampling verification in one pass).  The CTAs agree without
-//            communicating (same inputs, same reduction order); CTA 0 writes the outputs.
-//            Sampled requests then draw the token at the accepted length a, from
+//            (request, row, vocabulary chunk) tasks in request-major order, one contiguous range
+//            per CTA; one producer lane issues 1-D bulk copies (cp.async.bulk) of <= 16 KB chunks
+//            into a 4-stage shared-memory ring and eight consumer warps reduce each chunk.  A
+//            piece of a row (its chunks inside one CTA's range) becomes one record {max m,
+//            sum of 2^(x k - rint(m k)) with k = log2(e)/T, first argmax, logit at the drafted
+//            token}.  The kernel only streams and writes records: no atomics, no fences, no
+//            waiting on other CTAs.
+// combine    One CTA per request, launched behind row_stats with programmatic dependent launch.
+//            Merges the request's records into row statistics and runs the accept chain: the
+//            greedy test x_k == argmax, or the rejection test u_k q_k(x_k) < p_k(x_k); the first
+//            rejection is the accepted length (AngelSpec explainer, "MTP: fix position 2 and 3",
+//            eq. L_e2e: one rejection voids every later position; AngelSpec release article, "Why
+//            one universal drafter underperforms": rejection-sampling verification in one pass).
+// mass       One CTA per (request, vocabulary chunk): chunk sums of the residual
+//            max(0, p_a - q_a) after a rejection and of the target weights p_a.
+// pick       One CTA per request: the token at the accepted length a, drawn from
 //            norm(max(0, p_a - q_a)) after a rejection or from p_n when every drafted token was
-//            accepted (the bonus row), by inverse CDF in vocabulary order.  After a rejection
-//            each CTA sums the residual over its chunk (per chunk and per warp range) and the
-//            request's last CTA (one acquire-release counter) finds the crossing chunk, the
-//            crossing range, and scans ~1/8 of one chunk with one warp.  Bonus requests reuse
-//            row_stats' chunk sums and recompute one chunk.
+//            accepted (the bonus row), by inverse CDF in vocabulary order: a warp finds the
+//            crossing chunk from the chunk sums, the whole CTA scans that chunk.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -43,12 +41,6 @@ constexpr uint16_t kInfoInvalid = 1u << 12;
 
 // log2(e) / T in float; every kernel uses this one value for a request's temperature.
 __device__ __forceinline__ float kscale_of(float T) { return __fdiv_rn(kLog2eF, T); }
-
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 __device__ __forceinline__ int64_t target_row(const VerifyParams& p, int i, int k) {
   return (p.t_off ? static_cast<int64_t>(__ldg(p.t_off + i)) : static_cast<int64_t>(i) * (p.Kmax + 1)) + k;
@@ -316,6 +308,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   const char* rowp = nullptr;
   bool sampled = false;
   float kscale = 0.0f, m = -INFINITY, sacc = 0.0f, xfirst = NAN;
+  float cofs = 0.0f;  // exp_offset(m, kscale) of the running max (sampled rows)
   int g = -1, tok = -1, c_first = 0;
   for (int64_t t = t0; t < t1; ++t) {
     if (!row_open) {
@@ -438,32 +431,38 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
                                fmaxf(__uint_as_float(raw[j].z), __uint_as_float(raw[j].w))));
       }
       mc = fmaxf(mc, fmaxf(head_x, tail_x));
-      if (mc > m) {
-        sacc = (m == -INFINITY) ? 0.0f : sacc * ex2_approx((m - mc) * kscale);
+      if (mc > m) {  // new running max: move the running sum to the new offset (exact)
+        const float cnew = exp_offset(mc, kscale);
+        sacc = (m == -INFINITY) ? 0.0f : sacc * pow2_nonpos(cofs - cnew);
         m = mc;
+        cofs = cnew;
       }
       if (m != -INFINITY) {
-        float acc = 0.0f;
+        // terms 2^(x k - c): one fused multiply-add per logit, done on pairs of logits in
+        // packed f32x2 registers; even and odd positions keep separate sums
+        const f32x2 k2 = f2_pack(kscale, kscale), nc2 = f2_pack(-cofs, -cofs);
+        f32x2 acc2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < kVecPerThread; ++j) {
           if (tid + j * kConsumerThreads < nvec) {
             if constexpr (DT == SV_BF16) {
               const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                acc += ex2_approx((bf16_lo(w[e]) - m) * kscale);
-                acc += ex2_approx((bf16_hi(w[e]) - m) * kscale);
-              }
+              for (int e = 0; e < 4; ++e)
+                acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), k2, nc2));
             } else {
-              acc += ex2_approx((__uint_as_float(raw[j].x) - m) * kscale);
-              acc += ex2_approx((__uint_as_float(raw[j].y) - m) * kscale);
-              acc += ex2_approx((__uint_as_float(raw[j].z) - m) * kscale);
-              acc += ex2_approx((__uint_as_float(raw[j].w) - m) * kscale);
+              acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(__uint_as_float(raw[j].x), __uint_as_float(raw[j].y)),
+                                                 k2, nc2));
+              acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(__uint_as_float(raw[j].z), __uint_as_float(raw[j].w)),
+                                                 k2, nc2));
             }
           }
         }
-        if (has_head) acc += ex2_approx((head_x - m) * kscale);
-        if (has_tail) acc += ex2_approx((tail_x - m) * kscale);
+        float a0, a1;
+        f2_unpack(acc2, a0, a1);
+        float acc = a0 + a1;
+        if (has_head) acc += ex2_approx(__fmaf_rn(head_x, kscale, -cofs));
+        if (has_tail) acc += ex2_approx(__fmaf_rn(tail_x, kscale, -cofs));
         sacc += acc;
       }
     }
@@ -536,7 +535,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 // ------------------------------------------------------------------------------------------
 // Per-row statistics in shared memory (one entry per record row of the request).
 struct RowStatS {
-  float s;     // sum of 2^((x - m) k) over the row
+  float s;     // sum of 2^(x k - rint(m k)) over the row (sampled rows)
   float m;     // row max
   int32_t g;   // first argmax (greedy rows)
   float xval;  // logit at the row's drafted token (sampled rows)
@@ -572,9 +571,9 @@ struct PickSmem {
 template <int DT>
 __device__ __forceinline__ float draw_weight(const char* trow, const char* drow, int64_t v, bool residual,
                                              const ReqState& st) {
-  const float pv = ex2_approx((load_logit<DT>(trow, v) - st.mt) * st.kscale);
+  const float pv = ex2_approx(__fmaf_rn(load_logit<DT>(trow, v), st.kscale, -st.ct));
   if (!residual) return pv;
-  return fmaxf(0.0f, pv * st.inv_st - ex2_approx((load_logit<DT>(drow, v) - st.md) * st.kscale) * st.inv_sd);
+  return fmaxf(0.0f, pv * st.inv_st - ex2_approx(__fmaf_rn(load_logit<DT>(drow, v), st.kscale, -st.cd)) * st.inv_sd);
 }
 
 // Contiguous ranges of a chunk, one per warp: warp w of nw covers [lo, hi).
@@ -595,9 +594,9 @@ __device__ void warp_range_sum(const char* trow, const char* drow, int c0, int l
   constexpr int kVec = 16 / kElt;
   float acc_r = 0.0f, acc_p = 0.0f;
   auto add = [&](float tx, float dx) {
-    const float pv = ex2_approx((tx - st.mt) * st.kscale);
+    const float pv = ex2_approx(__fmaf_rn(tx, st.kscale, -st.ct));
     acc_p += pv;
-    if (residual) acc_r += fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx - st.md) * st.kscale) * st.inv_sd);
+    if (residual) acc_r += fmaxf(0.0f, pv * st.inv_st - ex2_approx(__fmaf_rn(dx, st.kscale, -st.cd)) * st.inv_sd);
   };
   const int len = hi - lo;
   const ChunkSplit a = split_chunk<kElt>(trow, c0 + lo, len);
@@ -709,8 +708,9 @@ __device__ int block_pick(const char* trow, const char* drow, int c0, int len, b
       for (int e = 0; e < kVec; ++e) {
         const int j = u * kVec + e;
         if (j < kMaxPer && j < cnt) {
-          const float pv = ex2_approx((tx[e] - st.mt) * st.kscale);
-          w[j] = residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx((dx[e] - st.md) * st.kscale) * st.inv_sd) : pv;
+          const float pv = ex2_approx(__fmaf_rn(tx[e], st.kscale, -st.ct));
+          w[j] = residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx(__fmaf_rn(dx[e], st.kscale, -st.cd)) * st.inv_sd)
+                          : pv;
         }
       }
     }
@@ -882,9 +882,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       float hi = 0.0f, lo = 0.0f;
       if (m != -INFINITY) {
+        const float C = exp_offset(m, kscale);
         for (int cc = lane; cc < NC; cc += 32) {
           const ChunkRecord rc = FL.staged ? rr[cc] : ld_record(rr + cc);
-          if (rc.m != -INFINITY) two_sum_acc(hi, lo, rc.s * exp2f((rc.m - m) * kscale));
+          if (rc.m != -INFINITY) two_sum_acc(hi, lo, rc.s * pow2_nonpos(exp_offset(rc.m, kscale) - C));
         }
       }
 #pragma unroll
@@ -936,8 +937,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       qv = 1.0f;
     } else {
       const RowStatS rt = rs[k], rd = rs[Kmax + 1 + k];
-      pv = __fdiv_rn(exp2f((rt.xval - rt.m) * kscale), rt.s);
-      qv = __fdiv_rn(exp2f((rd.xval - rd.m) * kscale), rd.s);
+      // row sums are of 2^(x k - c(row max)): the drafted token's term uses the same offset
+      pv = __fdiv_rn(exp2f(__fmaf_rn(rt.xval, kscale, -exp_offset(rt.m, kscale))), rt.s);
+      qv = __fdiv_rn(exp2f(__fmaf_rn(rd.xval, kscale, -exp_offset(rd.m, kscale))), rd.s);
       const float u = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 0u, p.round);
       acc = u * qv < pv;
       if (qv == 0.0f) atomicOr(&sm.acc_flags, SV_FLAG_Q_ZERO);
@@ -981,12 +983,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       st.flags = static_cast<int32_t>(sm.acc_flags);
       st.row_t = target_row(p, i, a);
       st.kscale = kscale;
-      st.mt = rs[a].m;
+      st.ct = exp_offset(rs[a].m, kscale);
       st.st = rs[a].s;
       st.inv_st = __frcp_rn(rs[a].s);
       if (a < n) {
         st.row_d = draft_row(p, i, a);
-        st.md = rs[Kmax + 1 + a].m;
+        st.cd = exp_offset(rs[Kmax + 1 + a].m, kscale);
         st.inv_sd = __frcp_rn(rs[Kmax + 1 + a].s);
       }
       st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);

@@ -144,6 +144,40 @@ def test_schedule_large_batch_limits():
     assert np.array_equal(keep.cpu().numpy(), o["keep_len"])
 
 
+def test_schedule_many_requests_per_thread_and_no_drafts():
+    rng = np.random.default_rng(4)
+    B, D = 3000, 5                                # 15000 slots, several requests per thread
+    alpha = rng.beta(4, 2, (B, D)).astype(np.float32)
+    dl = rng.integers(0, D + 1, B).astype(np.int32)
+    for budget, draft_len in ((0, None), (4000, dl)):
+        keep, offs, K, U = sv.schedule_depth(f32(alpha), 1.0, 0.02, budget, draft_len=None if draft_len is None
+                                             else i32(draft_len))
+        o = dcut_schedule(alpha, draft_len, 1.0, 0.02, budget)
+        assert int(K.item()) == o["K"] and int(U.item()) == o["U_q48"]
+        assert np.array_equal(keep.cpu().numpy(), o["keep_len"])
+        assert np.array_equal(offs.cpu().numpy(), np.concatenate([[0], np.cumsum(o["keep_len"] + 1)]))
+    a0 = torch.zeros((8, 0), dtype=torch.float32, device="cuda")   # Dmax = 0: roots only
+    keep, offs, K, U = sv.schedule_depth(a0, 1.0, 0.02, 0)
+    assert int(K.item()) == 8 and int(U.item()) == 8 << 48
+    assert keep.cpu().numpy().tolist() == [0] * 8
+
+
+def test_schedule_invalid_confidences_and_lengths():
+    alpha = np.full((6, 4), 0.5, np.float32)
+    for bad_alpha, dl, bit in ((1.5, None, 1 << 5), (np.nan, None, 1 << 5), (None, [1, 2, 5, 0, 4, 4], 1 << 6)):
+        a = alpha.copy()
+        if bad_alpha is not None:
+            a[3, 1] = bad_alpha
+        ws = sv.workspace(sv.SV_OP_SCHEDULE, 6, 4, 1, sv.SV_F32)
+        keep, offs, K, U = sv.schedule_depth(f32(a), 1.0, 0.02, 0, draft_len=None if dl is None
+                                             else i32(np.array(dl, np.int32)), ws=ws)
+        torch.cuda.synchronize()
+        assert int(K.item()) == -1 and int(U.item()) == -1
+        assert keep.cpu().numpy().tolist() == [0] * 6
+        assert offs.cpu().numpy().tolist() == list(range(7))
+        assert _status(ws) & bit
+
+
 def test_schedule_then_ragged_verify_on_device():
     """D-cut picks the kept prefixes on the device; the ragged verify consumes them without a
     host round trip (Figure 3 panels 3-4 of the D-cut section)."""
