@@ -319,6 +319,7 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
   p.budget = budget;
   p.objective = objective;
   p.sort_size = P;
+  p.merge = static_cast<int64_t>(B) * Dmax <= sv::kMergeMaxSlots ? 1 : 0;
   p.out_keep_len = out_keep_len;
   p.out_row_offsets = out_row_offsets;
   p.out_total_K = out_total_K;

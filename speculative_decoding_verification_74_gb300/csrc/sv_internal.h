@@ -10,7 +10,8 @@ namespace sv {
 // ---- row_stats kernel geometry ---------------------------------------------------------------
 constexpr int kStageBytes = 16384;     // one vocabulary chunk per pipeline stage
 constexpr int kStages = 4;             // bulk-copy ring depth
-constexpr int kConsumerWarps = 8;      // warps that reduce a chunk
+constexpr int kConsumerWarps = 4;      // warps that reduce a chunk (8 vectors per thread: the
+                                       // per-chunk bookkeeping is spread over 64 logits)
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kStatsThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;  // 16-byte vectors per thread
@@ -73,6 +74,10 @@ struct VerifyParams {
   int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
 };
 
+// Largest B * Dmax ranked by merging the per-request runs (two key buffers in shared memory);
+// larger batches use the bitonic sort, which is faster there on one CTA.
+constexpr int kMergeMaxSlots = 2048;
+
 struct ScheduleParams {
   const float* alpha;
   int32_t alpha_stride;
@@ -83,7 +88,8 @@ struct ScheduleParams {
   int32_t n_ratios;
   float ratios[8];
   int32_t objective;
-  int32_t sort_size;  // power of two >= B * Dmax (or 1)
+  int32_t sort_size;  // bitonic mode: power of two >= B * Dmax, at least 1024
+  int32_t merge;      // 1: merge the per-request runs (B * Dmax <= kMergeMaxSlots), 0: bitonic sort
   int32_t* out_keep_len;
   int32_t* out_row_offsets;
   int32_t* out_total_K;

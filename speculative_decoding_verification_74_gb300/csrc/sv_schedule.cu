@@ -9,10 +9,11 @@
 //   U(K) = sum of round(s * 2^48) over the kept slots (exact int64, order independent)
 //   pick the K maximising U / c(K) (or U - c(K)), c(K) = a + b K; ties -> smaller K
 // The ranking is a bitonic sort of 64-bit keys (~bits(s) : request : position) in shared
-// memory; with s >= 0 the float bits order like unsigned integers.  U(K) for every candidate
-// comes from one integer prefix scan of the sorted order.
+// memory, or (up to 8192 slots) a merge of the per-request runs, which are already in order;
+// with s >= 0 the float bits order like unsigned integers.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -131,44 +132,8 @@ __device__ void bitonic_sort(unsigned long long* keys, int P) {
   __syncthreads();
 }
 
-// Inclusive scan, across the CTA, of E 64-bit values per thread: thread t's value e belongs to
-// row e at column t (element e * kSchedThreads + t of the sorted order).  On return v[e] holds
-// the inclusive prefix within its row and row_tot[e] row e's total.
-template <int E>
-__device__ void block_row_scan64(long long (&v)[E], long long* wtot, long long* row_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xFFFFFFFFu, v[e], o);
-      if (lane >= o) v[e] += y;
-    }
-    if (lane == 31) wtot[e * 32 + warp] = v[e];
-  }
-  __syncthreads();
-  if (warp == 0) {
-    for (int e = 0; e < E; ++e) {
-      const long long w = wtot[e * 32 + lane];
-      long long wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-        if (lane >= o) wi += y;
-      }
-      wtot[e * 32 + lane] = wi - w;  // exclusive prefix of the warp totals
-      if (lane == 31) row_tot[e] = wi;
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int e = 0; e < E; ++e) v[e] += wtot[e * 32 + warp];
-}
-
 struct SchedSmem {
-  long long wtot[16 * 32];
-  long long row_tot[16];
-  long long ucand[8];
+  long long usum[8];
   double obj[8];
   int cand[8];
   int ncand;
@@ -176,63 +141,165 @@ struct SchedSmem {
   unsigned int bad;
 };
 
-// Sort, then U(K) of every candidate, the objective, and the chosen K (same in every thread).
-template <int E>
-__device__ void sort_and_choose(const ScheduleParams& p, unsigned long long* keys, int P, int B, SchedSmem& sm,
-                                int* Kb, long long* Ub) {
-  const int tid = threadIdx.x;
-  // ascending key == (s desc, request asc, position asc)
-  bitonic_sort<E>(keys, P);
-  const int nc = sm.ncand;  // written by thread 0 before the sort's barriers
+// ceil(r * N) for a float 0 < r <= 1 and 0 <= N < 2^31, exactly, in integer arithmetic
+// (r = mant * 2^-sh with sh >= 23; mant * N < 2^56).
+__device__ __forceinline__ int ceil_ratio_times(float r, int N) {
+  const uint32_t b = __float_as_uint(r);
+  const int ex = static_cast<int>((b >> 23) & 0xFF);
+  const uint64_t mant = (b & 0x7FFFFFu) | (ex ? 0x800000u : 0u);
+  const int sh = 150 - (ex ? ex : 1);
+  const uint64_t prod = mant * static_cast<uint64_t>(N);
+  if (prod == 0) return 0;
+  if (sh >= 64) return 1;
+  return static_cast<int>((prod + ((1ull << sh) - 1)) >> sh);
+}
 
-  // U(K) = sum of round(s * 2^48) over the first K - B sorted slots: one scan of the sorted
-  // order, read at each candidate (exact integer sums)
-  long long v[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) v[e] = q48_of_key(keys[e * kSchedThreads + tid]);  // padding gives 0
-  block_row_scan64<E>(v, sm.wtot, sm.row_tot);
-  for (int c = 0; c < nc; ++c) {
-    const int L = sm.cand[c] - B;  // slots beyond the always-kept roots
-    if (L == 0) {
-      if (tid == 0) sm.ucand[c] = 0;
-    } else if (((L - 1) & (kSchedThreads - 1)) == tid) {
-      const int er = (L - 1) / kSchedThreads;
-      long long u = 0;
-      for (int e = 0; e < er; ++e) u += sm.row_tot[e];
-#pragma unroll
-      for (int e = 0; e < E; ++e)
-        if (e == er) u += v[e];
-      sm.ucand[c] = u;
+// Candidate budgets (eq. K_rho) clipped to [B, cap], ascending, duplicates dropped (thread 0).
+__device__ void candidates(const ScheduleParams& p, int N, int B, SchedSmem& sm) {
+  const int cap = p.budget > 0 ? min(p.budget, N) : N;
+  int nc = 0;
+  for (int r = 0; r < p.n_ratios; ++r) {
+    const int K = max(min(max(ceil_ratio_times(p.ratios[r], N), B), cap), B);
+    bool dup = false;
+    for (int c = 0; c < nc; ++c) dup |= sm.cand[c] == K;
+    if (dup) continue;
+    int pos = nc++;
+    while (pos > 0 && sm.cand[pos - 1] > K) {
+      sm.cand[pos] = sm.cand[pos - 1];
+      --pos;
     }
+    sm.cand[pos] = K;
+  }
+  sm.ncand = nc;
+}
+
+// Merge sort of the B runs of Dmax keys (request q's keys, ascending along its positions) in
+// ceil(log2 B) levels.  At level 0 run q's key t sits at a[t * B + q] (position-major); later
+// levels hold runs contiguously.  A key of the left run of a pair lands at its index plus the
+// number of partner keys below it, a key of the right run at its index plus the number of
+// partner keys at or below it: a stable merge, so equal keys (the padding) stay valid.
+// Returns the buffer holding the sorted keys.
+__device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long long* b, int B, int Dmax) {
+  const int tid = threadIdx.x;
+  const int n = B * Dmax;
+  if (B <= 1) return a;  // one run: position-major is already contiguous
+  // level 0: pairs of single requests; threads walk the position-major order
+  for (int jj = tid; jj < n; jj += kSchedThreads) {
+    const int t = jj / B, q = jj - t * B;
+    const unsigned long long x = a[jj];
+    const int pq = q ^ 1;
+    int cnt = 0;
+    if (pq < B) {
+      const bool left = q < pq;
+      int lo = 0, len = Dmax;
+      while (len > 0) {
+        const int half = len >> 1;
+        const unsigned long long v = a[(lo + half) * B + pq];
+        if (left ? v < x : v <= x) {
+          lo += half + 1;
+          len -= half + 1;
+        } else {
+          len = half;
+        }
+      }
+      cnt = lo;
+    }
+    b[(pq < B ? min(q, pq) : q) * Dmax + t + cnt] = x;
+  }
+  __syncthreads();
+  unsigned long long* src = b;
+  unsigned long long* dst = a;
+  for (int lvl = 1; (1 << lvl) < B; ++lvl) {
+    for (int j = tid; j < n; j += kSchedThreads) {
+      const int q = j / Dmax;
+      const int r = q >> lvl, pr = r ^ 1;
+      const int rq = r << lvl, pq = pr << lvl;
+      const unsigned long long x = src[j];
+      if (pq >= B) {  // no partner run at this level
+        dst[j] = x;
+        continue;
+      }
+      const bool left = r < pr;
+      const int pbase = pq * Dmax;
+      int lo = 0, len = (min(pq + (1 << lvl), B) - pq) * Dmax;
+      while (len > 0) {
+        const int half = len >> 1;
+        const unsigned long long v = src[pbase + lo + half];
+        if (left ? v < x : v <= x) {
+          lo += half + 1;
+          len -= half + 1;
+        } else {
+          len = half;
+        }
+      }
+      dst[min(rq, pq) * Dmax + (j - rq * Dmax) + lo] = x;
+    }
+    __syncthreads();
+    unsigned long long* t = src;
+    src = dst;
+    dst = t;
+  }
+  return src;
+}
+
+// U(K) of every candidate (exact integer sums over the first K - B sorted keys), the
+// objective, and the chosen K (same in every thread).
+__device__ void choose(const ScheduleParams& p, const unsigned long long* sorted, int n, int B, SchedSmem& sm,
+                       int* Kb, long long* Ub) {
+  const int tid = threadIdx.x;
+  const int nc = sm.ncand;
+  int lim[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) lim[c] = c < nc ? sm.cand[c] - B : 0;
+  long long part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int jmax = min(sm.cand[nc - 1] - B, n);  // the largest candidate's slots
+  for (int j = tid; j < jmax; j += kSchedThreads) {
+    const long long q = q48_of_key(sorted[j]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (j < lim[c]) part[c] += q;
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (c >= nc) break;
+    long long v = part[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if ((tid & 31) == 0 && v != 0)
+      atomicAdd(reinterpret_cast<unsigned long long*>(&sm.usum[c]), static_cast<unsigned long long>(v));
   }
   __syncthreads();
 
   // objective (float64 with explicit rounding: no contraction), one thread per candidate
   if (tid < nc) {
-    const long long U = sm.ucand[tid] + static_cast<long long>(B) * (1ll << 48);
+    const long long U = sm.usum[tid] + static_cast<long long>(B) * (1ll << 48);
     const double util = __dmul_rn(__ll2double_rn(U), kTwoM48);
     const double cost = __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(sm.cand[tid])));
     sm.obj[tid] = p.objective == SV_OBJ_NET ? __dsub_rn(util, cost) : __ddiv_rn(util, cost);
-    sm.ucand[tid] = U;
+    sm.usum[tid] = U;
   }
   __syncthreads();
   int bc = 0;  // ties -> the smaller K (candidates are ascending)
   for (int c = 1; c < nc; ++c)
     if (sm.obj[c] > sm.obj[bc]) bc = c;
   *Kb = sm.cand[bc];
-  *Ub = sm.ucand[bc];
+  *Ub = sm.usum[bc];
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int B = p.B, Dmax = p.Dmax, P = p.sort_size;
-  // keys [P]; kept flags [Dmax][B], position-major: request i's position k at (k - 1) * B + i
+  const int B = p.B, Dmax = p.Dmax, n = B * Dmax;
+  // merge mode: keys [n] (position-major) + second buffer [n]; bitonic mode: keys [P]; then one
+  // kept flag per slot, position-major: request i's position k at (k - 1) * B + i
+  const int P = p.sort_size;
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
-  uint8_t* kept = smem + static_cast<size_t>(P) * 8;
+  unsigned long long* keys2 = keys + n;
+  uint8_t* kept = smem + static_cast<size_t>(p.merge ? 2 * n : P) * 8;
   __shared__ SchedSmem sm;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) sm.bad = 0;
+  if (tid < 8) sm.usum[tid] = 0;
   __syncthreads();
 
   // 0. each thread owns a contiguous block of requests: their lengths and confidences (all Dmax
@@ -271,7 +338,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
     }
     local += Dc;
   }
-  for (int j = B * Dmax + tid; j < P; j += kSchedThreads) keys[j] = ~0ull;
+  if (!p.merge)
+    for (int j = n + tid; j < P; j += kSchedThreads) keys[j] = ~0ull;
   int wsum = local;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
@@ -293,45 +361,34 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
     return;
   }
 
-  // 1. candidate budgets (eq. K_rho) clipped to [B, cap], ascending, duplicates dropped.  Thread
-  //    0 computes them while the other threads start the sort; the sort's barriers publish them.
-  const int N = M + B;
-  if (tid == 0) {
-    const int cap = p.budget > 0 ? min(p.budget, N) : N;
-    int nc = 0;
-    for (int r = 0; r < p.n_ratios; ++r) {
-      int K = static_cast<int>(ceil(static_cast<double>(p.ratios[r]) * static_cast<double>(N)));
-      K = max(K, B);
-      K = min(K, cap);
-      K = max(K, B);
-      bool dup = false;
-      for (int c = 0; c < nc; ++c) dup |= sm.cand[c] == K;
-      if (dup) continue;
-      int pos = nc++;
-      while (pos > 0 && sm.cand[pos - 1] > K) {
-        sm.cand[pos] = sm.cand[pos - 1];
-        --pos;
-      }
-      sm.cand[pos] = K;
-    }
-    sm.ncand = nc;
-  }
+  // 1. candidate budgets: thread 0 computes them while the others start ranking (the ranking's
+  //    barriers publish them)
+  if (tid == 0) candidates(p, M + B, B, sm);
 
-  // 2-5. sort, utilities, objective, chosen K
-  int Kb = B;
-  long long Ub = 0;
-  switch (P / kSchedThreads) {
-    case 1: sort_and_choose<1>(p, keys, P, B, sm, &Kb, &Ub); break;
-    case 2: sort_and_choose<2>(p, keys, P, B, sm, &Kb, &Ub); break;
-    case 4: sort_and_choose<4>(p, keys, P, B, sm, &Kb, &Ub); break;
-    case 8: sort_and_choose<8>(p, keys, P, B, sm, &Kb, &Ub); break;
-    default: sort_and_choose<16>(p, keys, P, B, sm, &Kb, &Ub); break;
+  // 2-5. rank the non-root slots (s desc, request asc, position asc == ascending key), then
+  //      utilities, objective, chosen K
+  const unsigned long long* sorted;
+  if (p.merge) {
+    sorted = merge_runs(keys, keys2, B, Dmax);
+    if (B <= 1) __syncthreads();  // no merge level ran: publish the candidates
+  } else {
+    switch (P / kSchedThreads) {
+      case 1: bitonic_sort<1>(keys, P); break;
+      case 2: bitonic_sort<2>(keys, P); break;
+      case 4: bitonic_sort<4>(keys, P); break;
+      case 8: bitonic_sort<8>(keys, P); break;
+      default: bitonic_sort<16>(keys, P); break;
+    }
+    sorted = keys;
   }
+  int Kb;
+  long long Ub;
+  choose(p, sorted, p.merge ? n : P, B, sm, &Kb, &Ub);
 
   // 6. kept slots: the first Kb - B sorted keys, marked at their (position, request) place; a
   //    request's kept slots are a prefix of its positions, so its depth is their count
   for (int j = tid; j < Kb - B; j += kSchedThreads) {
-    const unsigned long long key = keys[j];
+    const unsigned long long key = sorted[j];
     const int i = static_cast<int>((key >> 10) & 0x3FFFFFull), k = static_cast<int>(key & 0x3FFull);
     kept[static_cast<int64_t>(k - 1) * B + i] = 1;
   }
@@ -340,10 +397,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
   // 7. per-request kept depth and packed row offsets
   int loc = 0;
   for (int i = r0; i < r1; ++i) {
-    int n = 0;
-    for (int k = 0; k < Dmax; ++k) n += kept[static_cast<int64_t>(k) * B + i];
-    p.out_keep_len[i] = n;
-    loc += n + 1;
+    int cnt = 0;
+    for (int k = 0; k < Dmax; ++k) cnt += kept[static_cast<int64_t>(k) * B + i];
+    p.out_keep_len[i] = cnt;
+    loc += cnt + 1;
   }
   int rexcl;
   const int rtot = block_exclusive_scan(loc, &rexcl, sm.warp_tot);
@@ -366,8 +423,9 @@ bool g_sched_attr_set = false;
 
 int launch_schedule(const ScheduleParams& p, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // sort keys, then one kept flag per slot
-  const size_t dyn = static_cast<size_t>(p.sort_size) * 8 + static_cast<size_t>(p.B) * p.Dmax;
+  // sort keys (two buffers when merging), then one kept flag per slot
+  const size_t n = static_cast<size_t>(p.B) * p.Dmax;
+  const size_t dyn = (p.merge ? 2 * n : static_cast<size_t>(p.sort_size)) * 8 + n;
   cudaError_t e;
   if (!g_sched_attr_set) {
     const int max_dyn = SV_MAX_SCHEDULE_SLOTS * 8 + SV_MAX_SCHEDULE_SLOTS;

@@ -3,7 +3,7 @@
 // row_stats  One streaming pass over every logit row a round needs.  A persistent grid walks
 //            (request, row, vocabulary chunk) tasks in request-major order, one contiguous range
 //            per CTA; one producer lane issues 1-D bulk copies (cp.async.bulk) of <= 16 KB chunks
-//            into a 4-stage shared-memory ring and eight consumer warps reduce each chunk.  A
+//            into a 4-stage shared-memory ring and four consumer warps reduce each chunk.  A
 //            piece of a row (its chunks inside one CTA's range) becomes one record {max m,
 //            sum of 2^(x k - rint(m k)) with k = log2(e)/T, first argmax, logit at the drafted
 //            token}.  The kernel only streams and writes records: no atomics, no fences, no
@@ -140,6 +140,18 @@ struct RowRef {
   bool is_target;
 };
 
+// Request holding row r: the largest i in [0, B) with row_start[i] <= r (a request without rows
+// shares its start with the next request and is never the largest).
+__device__ __forceinline__ int find_request(const int* row_start, int B, int r) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (row_start[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 __device__ __forceinline__ void locate_row(const int* row_start, const uint16_t* info, int Kmax, int row, int& i,
                                            RowRef& rr) {
   while (row >= row_start[i + 1]) ++i;  // rows are visited in increasing order
@@ -256,7 +268,8 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   if (tid >= kConsumerThreads) {
     // ---------------- producer warp: one lane issues the bulk copies ----------------
     if (tid == kConsumerThreads) {
-      int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
+      int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC);
+      int i = uniform ? 0 : find_request(row_start, B, row);
       RowRef rr;
       locate(row, i, rr);
       const char* src = row_base<DT>(p, rr);
@@ -298,7 +311,8 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   }
 
   // ---------------- consumer warps ----------------
-  int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC), i = 0;
+  int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC);
+  int i = uniform ? 0 : find_request(row_start, B, row);
   RowRef rr;
   locate(row, i, rr);
   uint32_t it = 0;
@@ -505,7 +519,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
         float ss = lane < kConsumerWarps ? red[buf].s[lane] : 0.0f;
         int gg = lane < kConsumerWarps ? red[buf].g[lane] : -1;
 #pragma unroll
-        for (int o = 4; o > 0; o >>= 1) {
+        for (int o = kConsumerWarps / 2; o > 0; o >>= 1) {
           const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mm, o);
           const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ss, o);
           const int g2 = __shfl_xor_sync(0xFFFFFFFFu, gg, o);

@@ -162,6 +162,24 @@ def test_schedule_many_requests_per_thread_and_no_drafts():
     assert keep.cpu().numpy().tolist() == [0] * 8
 
 
+@pytest.mark.parametrize("B,D", [(1, 7), (2, 5), (3, 4), (5, 16), (33, 7), (37, 20), (128, 16), (683, 3), (512, 16)])
+def test_schedule_run_merge_shapes(B, D):
+    """Batch shapes around the ranking's cases: one run, odd run counts (a run without a partner
+    at some merge level), the largest merged size (128 x 16 = 2048 slots), the first size ranked
+    by the bitonic sort (683 x 3 = 2049 slots) and a larger one; confidences with many ties."""
+    rng = np.random.default_rng(B * 100 + D)
+    ties = rng.choice(np.array([0.0, 0.5, 0.5, 0.9, 1.0], np.float32), size=(B, D))
+    alpha = np.where(rng.random((B, D)) < 0.5, ties, rng.beta(6, 2, (B, D)).astype(np.float32)).astype(np.float32)
+    dl = rng.integers(0, D + 1, B).astype(np.int32)
+    for draft_len, budget in ((None, 0), (dl, max(B, (B * D) // 3))):
+        keep, offs, K, U = sv.schedule_depth(f32(alpha), 0.8, 0.03, budget,
+                                             draft_len=None if draft_len is None else i32(draft_len))
+        o = dcut_schedule(alpha, draft_len, 0.8, 0.03, budget)
+        assert int(K.item()) == o["K"] and int(U.item()) == o["U_q48"]
+        assert np.array_equal(keep.cpu().numpy(), o["keep_len"])
+        assert np.array_equal(offs.cpu().numpy(), np.concatenate([[0], np.cumsum(o["keep_len"] + 1)]))
+
+
 def test_schedule_invalid_confidences_and_lengths():
     alpha = np.full((6, 4), 0.5, np.float32)
     for bad_alpha, dl, bit in ((1.5, None, 1 << 5), (np.nan, None, 1 << 5), (None, [1, 2, 5, 0, 4, 4], 1 << 6)):
