@@ -262,11 +262,11 @@ const char* sv_last_error_string(void);
  * brackets.  sv_launch_count returns the number of library kernel launches (or
  * captured launch nodes) since the library was loaded. */
 enum {
-  SV_KERNEL_ROW_STATS = 0,
-  SV_KERNEL_COMBINE = 1,
-  SV_KERNEL_SCHEDULE = 2,
-  SV_KERNEL_MASS = 3,
-  SV_KERNEL_PICK = 4,
+  SV_KERNEL_ROW_STATS = 0, /* streaming pass over the logit rows                          */
+  SV_KERNEL_COMBINE = 1,   /* accept chain (+ per-chunk draw weights for short requests)  */
+  SV_KERNEL_SCHEDULE = 2,  /* D-cut depth allocation                                      */
+  SV_KERNEL_MASS = 3,      /* per-chunk draw weights for long requests                    */
+  SV_KERNEL_PICK = 4,      /* inverse-CDF draw                                            */
   SV_NUM_KERNELS = 5
 };
 void sv_profile_enable(int on);

@@ -72,6 +72,7 @@ struct VerifyParams {
   float* mass;              // [B * nchunks] residual mass per chunk
   float* mass_p;            // [B * nchunks] target-row weight per chunk (bonus draw / fallback)
   int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
+  int32_t fuse_draw;        // 1: the combine kernel's CTAs also sum the draw weights per chunk
 };
 
 // Largest B * Dmax ranked by merging the per-request runs (two key buffers in shared memory);

@@ -8,14 +8,17 @@
 //            sum of 2^(x k - rint(m k)) with k = log2(e)/T, first argmax, logit at the drafted
 //            token}.  The kernel only streams and writes records: no atomics, no fences, no
 //            waiting on other CTAs.
-// combine    One CTA per request, launched behind row_stats with programmatic dependent launch.
-//            Merges the request's records into row statistics and runs the accept chain: the
-//            greedy test x_k == argmax, or the rejection test u_k q_k(x_k) < p_k(x_k); the first
-//            rejection is the accepted length (AngelSpec explainer, "MTP: fix position 2 and 3",
-//            eq. L_e2e: one rejection voids every later position; AngelSpec release article, "Why
+// combine    Launched behind row_stats with programmatic dependent launch, grid (vocabulary
+//            chunks, B) for short sampled requests, else (1, B).  Every CTA of request i merges the
+//            request's records into row statistics and runs the accept chain: the greedy test
+//            x_k == argmax, or the rejection test u_k q_k(x_k) < p_k(x_k); the first rejection
+//            is the accepted length (AngelSpec explainer, "MTP: fix position 2 and 3", eq.
+//            L_e2e: one rejection voids every later position; AngelSpec release article, "Why
 //            one universal drafter underperforms": rejection-sampling verification in one pass).
-// mass       One CTA per (request, vocabulary chunk): chunk sums of the residual
-//            max(0, p_a - q_a) after a rejection and of the target weights p_a.
+//            CTA 0 writes the outputs; each CTA of a short sampled request then sums its chunk of
+//            the residual max(0, p_a - q_a) after a rejection and of the target weights p_a.
+// mass       For longer requests the same chunk sums come from a separate grid (chunks, B) that
+//            reads the draw state the combine leaves.
 // pick       One CTA per request: the token at the accepted length a, drawn from
 //            norm(max(0, p_a - q_a)) after a rejection or from p_n when every drafted token was
 //            accepted (the bonus row), by inverse CDF in vocabulary order: a warp finds the
@@ -559,6 +562,10 @@ constexpr size_t kFinMaxStagedBytes = 48 * 1024;  // chunk records staged in sha
 constexpr int kFinMaxDynSmem = 96 * 1024;
 constexpr int kCombineThreads = 256, kCombineWarps = kCombineThreads / 32;
 constexpr int kMassThreads = 128, kMassWarps = kMassThreads / 32;
+// Requests with at most this many chunk records (rows x chunks) get their draw weights summed by
+// the combine kernel's CTAs, which each merge the request's records again; longer requests use
+// the separate mass kernel, which reads the draw state the combine leaves.
+constexpr int kFuseDrawMaxRecords = 256;
 constexpr int kPickThreads = 256, kPickWarps = kPickThreads / 32;
 constexpr int kPickStagedChunks = 2048;  // chunk masses staged in shared memory up to this many
 
@@ -831,14 +838,21 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// ---- combine: one CTA per request --------------------------------------------------------
+// ---- combine: grid (chunks, B) when the draw weights are fused in, (1, B) otherwise -------
+// Every CTA of request i merges the request's records and runs its accept chain (the CTAs agree
+// without communicating: same inputs, same order of operations); CTA 0 writes the outputs and
+// the draw state.  With the draw weights fused in, each CTA of a sampled request then sums its
+// vocabulary chunk of the residual max(0, p_a - q_a) after a rejection, and of the target
+// weights p_a (the bonus draw, or the fallback when the residual mass is zero).
 template <int DT>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyParams p) {
   extern __shared__ __align__(16) unsigned char fin_dyn[];
   __shared__ CombineSmem sm;
+  __shared__ ReqState sst;
+  __shared__ float wr_s[kCombineWarps], wp_s[kCombineWarps];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x;
+  const int i = blockIdx.y, c = blockIdx.x;
   const int NC = p.nchunks, R = p.rows_per_req, Kmax = p.Kmax;
   const FinLayout FL = fin_layout(R, NC, Kmax);
   RowStatS* rs = reinterpret_cast<RowStatS*>(fin_dyn);                        // [R]
@@ -859,12 +873,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
   cp_async_wait_all();
   __syncthreads();
+  if (c > 0 && !(info & kInfoSampled)) return;  // nothing to draw: CTA 0 does all the work
   if (info & kInfoInvalid) {
-    if (tid == 0) {
-      atomicOr(p.status, bad_in);
-      p.req[i].mode = kModeNone;
+    if (c == 0) {
+      if (tid == 0) {
+        atomicOr(p.status, bad_in);
+        p.req[i].mode = kModeNone;
+      }
+      write_invalid(p, i, tid, kCombineThreads);
     }
-    write_invalid(p, i, tid, kCombineThreads);
     return;
   }
   const int n = info & kInfoN;
@@ -958,37 +975,45 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       acc = u * qv < pv;
       if (qv == 0.0f) atomicOr(&sm.acc_flags, SV_FLAG_Q_ZERO);
     }
-    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = pv;
-    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = qv;
+    if (c == 0) {
+      if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = pv;
+      if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = qv;
+    }
     if (!acc) atomicMin(&sm.a_min, k);
   }
-  for (int k = n + tid; k < Kmax; k += kCombineThreads) {
-    if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
-    if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
-  }
+  if (c == 0)
+    for (int k = n + tid; k < Kmax; k += kCombineThreads) {
+      if (p.out_p) p.out_p[static_cast<int64_t>(i) * Kmax + k] = NAN;
+      if (p.out_q) p.out_q[static_cast<int64_t>(i) * Kmax + k] = NAN;
+    }
   __syncthreads();
   if (sm.bad) {
-    if (tid == 0) {
-      atomicOr(p.status, sm.bad);
-      p.req[i].mode = kModeNone;
+    if (c == 0) {
+      if (tid == 0) {
+        atomicOr(p.status, sm.bad);
+        p.req[i].mode = kModeNone;
+      }
+      write_invalid(p, i, tid, kCombineThreads);
     }
-    write_invalid(p, i, tid, kCombineThreads);
     return;
   }
   const int a = sm.a_min;
 
-  // 3. emit: the accepted prefix (and, greedy, the target argmax at a); a sampled request's
-  //    token at a is written by the pick kernel
-  for (int j = tid; j <= Kmax; j += kCombineThreads) {
-    if (j == a && sampled) continue;
-    int v = -1;
-    if (j < a) v = tok(j);
-    else if (j == a) v = rs[a].g;
-    p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
-  }
+  // 3. emit (CTA 0): the accepted prefix (and, greedy, the target argmax at a); a sampled
+  //    request's token at a is written by the pick kernel
+  if (c == 0)
+    for (int j = tid; j <= Kmax; j += kCombineThreads) {
+      if (j == a && sampled) continue;
+      int v = -1;
+      if (j < a) v = tok(j);
+      else if (j == a) v = rs[a].g;
+      p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + j] = v;
+    }
   if (tid == 0) {
-    p.out_accept_len[i] = a;
-    if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(sm.acc_flags);
+    if (c == 0) {
+      p.out_accept_len[i] = a;
+      if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(sm.acc_flags);
+    }
     ReqState st = {};
     st.mode = kModeNone;
     if (sampled) {
@@ -1007,7 +1032,34 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       }
       st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
     }
-    p.req[i] = st;
+    if (c == 0) p.req[i] = st;
+    sst = st;
+  }
+  __syncthreads();
+  if (!p.fuse_draw || sst.mode == kModeNone) return;
+
+  // 4. this CTA's vocabulary chunk of the draw weights (row a of the request)
+  const bool residual = sst.mode == kModeResidual;
+  const char* trow = row_ptr<DT>(p.target, sst.row_t, p.t_row_stride);
+  const char* drow = residual ? row_ptr<DT>(p.draft, sst.row_d, p.d_row_stride) : trow;
+  const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+  int lo, hi;
+  warp_range(len, kCombineWarps, warp, &lo, &hi);
+  float wr, wp;
+  warp_range_sum<DT>(trow, drow, c0, lo, hi, residual, sst, lane, &wr, &wp);
+  if (lane == 0) {
+    wr_s[warp] = wr;
+    wp_s[warp] = wp;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float tr = 0.0f, tp = 0.0f;
+    for (int w = 0; w < kCombineWarps; ++w) {
+      tr += wr_s[w];
+      tp += wp_s[w];
+    }
+    p.mass[static_cast<int64_t>(i) * NC + c] = tr;
+    p.mass_p[static_cast<int64_t>(i) * NC + c] = tp;
   }
 }
 
@@ -1182,12 +1234,13 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
     g_fin_attr_set[di] = true;
   }
   const size_t csmem = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
-  if ((e = launch_pdl(combine_kernel<DT>, dim3(p.B), kCombineThreads, csmem, stream, SV_KERNEL_COMBINE, p)) !=
-      cudaSuccess)
+  if ((e = launch_pdl(combine_kernel<DT>, dim3(p.fuse_draw ? p.nchunks : 1, p.B), kCombineThreads, csmem, stream,
+                      SV_KERNEL_COMBINE, p)) != cudaSuccess)
     return e;
   if (!sampled) return cudaSuccess;
-  if ((e = launch_pdl(mass_kernel<DT>, dim3(p.nchunks, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p)) !=
-      cudaSuccess)
+  if (!p.fuse_draw &&
+      (e = launch_pdl(mass_kernel<DT>, dim3(p.nchunks, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p)) !=
+          cudaSuccess)
     return e;
   return launch_pdl(pick_kernel<DT>, dim3(p.B), kPickThreads, 0, stream, SV_KERNEL_PICK, p);
 }
@@ -1227,8 +1280,10 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   return L;
 }
 
-int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream) {
+int launch_verify(const VerifyParams& p_in, sv_dtype dt, bool sampled, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VerifyParams p = p_in;
+  p.fuse_draw = sampled && static_cast<int64_t>(p.rows_per_req) * p.nchunks <= kFuseDrawMaxRecords ? 1 : 0;
   return static_cast<int>(dt == SV_BF16 ? launch_verify_t<SV_BF16>(p, sampled, s)
                                         : launch_verify_t<SV_F32>(p, sampled, s));
 }

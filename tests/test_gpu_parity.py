@@ -84,6 +84,19 @@ def test_sample_small(name, seed):
     assert _status(ws) == 0
 
 
+@pytest.mark.parametrize("make", [lambda: W.c3_dfly(21, B=3, K=16, V=70001),     # 33 rows x 18 chunks
+                                  lambda: W.c2_mtp(22, B=4, K=12, V=90001)])      # 25 rows x 11 chunks
+def test_sample_long_requests_separate_draw_weights(make):
+    """Requests with more chunk records than the combine kernel re-merges per chunk: the draw
+    weights come from the separate per-chunk kernel."""
+    b = make()
+    tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, b.dtype), dev_rows(b.draft, b.dtype), i32(b.tokens),
+                                           f32(b.temperature), b.Kmax, seed=b.seed, round_=b.round,
+                                           request_ids=i32(b.request_ids))
+    torch.cuda.synchronize()
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len)
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2, 3])
 def test_ragged_mixed_small(seed):
     b = W.small("c5", seed)                      # mixed K in {3,16}, T in {0, 0.6, 1}, packed rows
