@@ -69,8 +69,8 @@ struct VerifyParams {
   uint32_t* status;
   ReqState* req;            // [B] draw state per request
   ChunkRecord* rec;         // [B * rows_per_req * nchunks]
-  float* mass;              // [B * nchunks] residual mass per chunk
-  float* mass_p;            // [B * nchunks] target-row weight per chunk (bonus draw / fallback)
+  float* mass;              // [B * nchunks * 8] residual mass per draw range (8 per chunk)
+  float* mass_p;            // [B * nchunks * 8] target-row weight per draw range (bonus / fallback)
   int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
   int32_t fuse_draw;        // 1: the combine kernel's CTAs also sum the draw weights per chunk
 };

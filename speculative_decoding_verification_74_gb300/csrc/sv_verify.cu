@@ -561,13 +561,17 @@ struct RowStatS {
 constexpr size_t kFinMaxStagedBytes = 48 * 1024;  // chunk records staged in shared memory up to this
 constexpr int kFinMaxDynSmem = 96 * 1024;
 constexpr int kCombineThreads = 256, kCombineWarps = kCombineThreads / 32;
-constexpr int kMassThreads = 128, kMassWarps = kMassThreads / 32;
+constexpr int kMassThreads = 256, kMassWarps = kMassThreads / 32;
+// Each vocabulary chunk's draw weights are summed in kDrawRanges contiguous ranges (one per
+// warp); the pick kernel finds the crossing range and scans only that range.
+constexpr int kDrawRanges = 8;
+static_assert(kCombineWarps == kDrawRanges && kMassWarps == kDrawRanges, "one draw range per warp");
 // Requests with at most this many chunk records (rows x chunks) get their draw weights summed by
 // the combine kernel's CTAs, which each merge the request's records again; longer requests use
 // the separate mass kernel, which reads the draw state the combine leaves.
 constexpr int kFuseDrawMaxRecords = 256;
 constexpr int kPickThreads = 256, kPickWarps = kPickThreads / 32;
-constexpr int kPickStagedChunks = 2048;  // chunk masses staged in shared memory up to this many
+constexpr int kPickStaged = 2048;  // range masses staged in shared memory up to this many
 
 struct CombineSmem {
   int a_min;
@@ -585,7 +589,7 @@ struct PickSmem {
   float thr;        // u' * Z
   int pick_thread;  // first thread whose entries hold the crossing
   int last_pos;     // broadcast of the pick
-  float mass[2 * kPickStagedChunks];
+  float mass[2 * kPickStaged];
 };
 
 // weight of vocabulary entry v of a row pair for the draw (target-only when !residual)
@@ -849,7 +853,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   extern __shared__ __align__(16) unsigned char fin_dyn[];
   __shared__ CombineSmem sm;
   __shared__ ReqState sst;
-  __shared__ float wr_s[kCombineWarps], wp_s[kCombineWarps];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.y, c = blockIdx.x;
@@ -1048,18 +1051,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   float wr, wp;
   warp_range_sum<DT>(trow, drow, c0, lo, hi, residual, sst, lane, &wr, &wp);
   if (lane == 0) {
-    wr_s[warp] = wr;
-    wp_s[warp] = wp;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float tr = 0.0f, tp = 0.0f;
-    for (int w = 0; w < kCombineWarps; ++w) {
-      tr += wr_s[w];
-      tp += wp_s[w];
-    }
-    p.mass[static_cast<int64_t>(i) * NC + c] = tr;
-    p.mass_p[static_cast<int64_t>(i) * NC + c] = tp;
+    const int64_t e = (static_cast<int64_t>(i) * NC + c) * kDrawRanges + warp;
+    p.mass[e] = wr;
+    p.mass_p[e] = wp;
   }
 }
 
@@ -1069,7 +1063,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
 template <int DT>
 __global__ void __launch_bounds__(kMassThreads) mass_kernel(const VerifyParams p) {
   __shared__ ReqState st;
-  __shared__ float wr_s[kMassWarps], wp_s[kMassWarps];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.y, c = blockIdx.x, NC = p.nchunks;
@@ -1085,18 +1078,9 @@ __global__ void __launch_bounds__(kMassThreads) mass_kernel(const VerifyParams p
   float wr, wp;
   warp_range_sum<DT>(trow, drow, c0, lo, hi, residual, st, lane, &wr, &wp);
   if (lane == 0) {
-    wr_s[warp] = wr;
-    wp_s[warp] = wp;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float tr = 0.0f, tp = 0.0f;
-    for (int w = 0; w < kMassWarps; ++w) {
-      tr += wr_s[w];
-      tp += wp_s[w];
-    }
-    p.mass[static_cast<int64_t>(i) * NC + c] = tr;
-    p.mass_p[static_cast<int64_t>(i) * NC + c] = tp;
+    const int64_t e = (static_cast<int64_t>(i) * NC + c) * kDrawRanges + warp;
+    p.mass[e] = wr;
+    p.mass_p[e] = wp;
   }
 }
 
@@ -1114,26 +1098,27 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
   const bool residual_mode = st.mode == kModeResidual;
   const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
   const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
-  const float* mass_r = p.mass + static_cast<int64_t>(i) * NC;
-  const float* mass_p = p.mass_p + static_cast<int64_t>(i) * NC;
-  const bool staged = NC <= kPickStagedChunks;
-  if (staged) {  // one round for every chunk mass of the request
-    for (int j = tid; j < NC; j += kPickThreads) {
+  const int NE = NC * kDrawRanges;  // draw ranges of the request, in vocabulary order
+  const float* mass_r = p.mass + static_cast<int64_t>(i) * NE;
+  const float* mass_p = p.mass_p + static_cast<int64_t>(i) * NE;
+  const bool staged = NE <= kPickStaged;
+  if (staged) {  // one round for every range mass of the request
+    for (int j = tid; j < NE; j += kPickThreads) {
       sm.mass[j] = mass_r[j];
-      sm.mass[kPickStagedChunks + j] = mass_p[j];
+      sm.mass[kPickStaged + j] = mass_p[j];
     }
   }
   __syncthreads();
 
-  // the crossing chunk (one warp)
+  // the crossing range (one warp)
   if (warp == 0) {
-    auto r_at = [&](int cc) { return staged ? sm.mass[cc] : mass_r[cc]; };
-    auto p_at = [&](int cc) { return staged ? sm.mass[kPickStagedChunks + cc] : mass_p[cc]; };
+    auto r_at = [&](int e) { return staged ? sm.mass[e] : mass_r[e]; };
+    auto p_at = [&](int e) { return staged ? sm.mass[kPickStaged + e] : mass_p[e]; };
     int bonus = residual_mode ? 0 : 1;
     uint32_t flags = 0;
     float Z = 0.0f;
     if (!bonus) {
-      for (int cc = lane; cc < NC; cc += 32) Z += r_at(cc);
+      for (int e = lane; e < NE; e += 32) Z += r_at(e);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
       if (!(Z > 0.0f)) {
@@ -1143,15 +1128,15 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
     }
     if (bonus) {
       Z = 0.0f;
-      for (int cc = lane; cc < NC; cc += 32) Z += p_at(cc);
+      for (int e = lane; e < NE; e += 32) Z += p_at(e);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xFFFFFFFFu, Z, o);
     }
     const float thr = st.u * Z;
     float before = 0.0f;
-    const int cstar = bonus ? warp_find(NC, thr, p_at, &before, lane) : warp_find(NC, thr, r_at, &before, lane);
+    const int estar = bonus ? warp_find(NE, thr, p_at, &before, lane) : warp_find(NE, thr, r_at, &before, lane);
     if (lane == 0) {
-      sm.chunk = cstar;
+      sm.chunk = estar;
       sm.base = before;
       sm.thr = thr;
       sm.bonus = bonus;
@@ -1159,13 +1144,17 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
     }
   }
   __syncthreads();
-  const int cstar = sm.chunk;
+
+  // the entry inside the crossing range (whole CTA)
+  const int estar = sm.chunk, cstar = estar / kDrawRanges;
   const bool residual = !sm.bonus;
-  const int c0 = cstar * p.chunk_len, len = min(p.chunk_len, p.V - c0);
-  int y = block_pick<DT>(trow, residual ? drow : trow, c0, len, residual, st, sm.thr - sm.base, &sm, tid);
+  const int c0 = cstar * p.chunk_len;
+  int lo, hi;
+  warp_range(min(p.chunk_len, p.V - c0), kDrawRanges, estar - cstar * kDrawRanges, &lo, &hi);
+  int y = block_pick<DT>(trow, residual ? drow : trow, c0 + lo, hi - lo, residual, st, sm.thr - sm.base, &sm, tid);
   if (tid == 0) {
-    if (y < 0) y = 0;  // only if every weight of the chunk flushed to zero; keep a valid token
-    p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + y;
+    if (y < 0) y = 0;  // only if every weight of the range flushed to zero; keep a valid token
+    p.out_tokens[static_cast<int64_t>(i) * (Kmax + 1) + st.a] = c0 + lo + y;
     if (p.out_flags && sm.flags) p.out_flags[i] = static_cast<uint8_t>(st.flags | sm.flags);
   }
 }
@@ -1271,9 +1260,9 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   L.req = off;
   off = align256(off + sizeof(ReqState) * B);
   L.mass = off;
-  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
+  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks) * kDrawRanges);
   L.mass_p = off;
-  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks));
+  off = align256(off + sizeof(float) * B * static_cast<size_t>(nchunks) * kDrawRanges);
   L.rec = off;
   off = align256(off + sizeof(ChunkRecord) * B * R * static_cast<size_t>(nchunks));
   L.total = off;
