@@ -400,30 +400,36 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
       for (int j = 0; j < kVecPerThread; ++j) {
         const int v = tid + j * kConsumerThreads;
         if (v < nvec) {
-          const int base = v0 + v * kVec;
+          // the vector's first argmax by a pairwise tree (the left element wins ties), then one
+          // merge into the running argmax: a short dependency chain per vector
+          float x[kVec];
           if constexpr (DT == SV_BF16) {
             const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
-              if (g < 0 || lo > m) {
-                m = lo;
-                g = base + 2 * e;
-              }
-              if (hi > m) {
-                m = hi;
-                g = base + 2 * e + 1;
-              }
+              x[2 * e] = bf16_lo(w[e]);
+              x[2 * e + 1] = bf16_hi(w[e]);
             }
           } else {
-            const float w[4] = {__uint_as_float(raw[j].x), __uint_as_float(raw[j].y),
-                                __uint_as_float(raw[j].z), __uint_as_float(raw[j].w)};
+            x[0] = __uint_as_float(raw[j].x);
+            x[1] = __uint_as_float(raw[j].y);
+            x[2] = __uint_as_float(raw[j].z);
+            x[3] = __uint_as_float(raw[j].w);
+          }
+          int ix[kVec];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (g < 0 || w[e] > m) {
-                m = w[e];
-                g = base + e;
+          for (int e = 0; e < kVec; ++e) ix[e] = e;
+#pragma unroll
+          for (int step = 1; step < kVec; step <<= 1)
+#pragma unroll
+            for (int e = 0; e + step < kVec; e += 2 * step)
+              if (x[e + step] > x[e]) {
+                x[e] = x[e + step];
+                ix[e] = ix[e + step];
               }
+          if (g < 0 || x[0] > m) {
+            m = x[0];
+            g = v0 + v * kVec + ix[0];
           }
         }
       }
@@ -458,7 +464,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
         // terms 2^(x k - c): one fused multiply-add per logit, done on pairs of logits in
         // packed f32x2 registers; even and odd positions keep separate sums
         const f32x2 k2 = f2_pack(kscale, kscale), nc2 = f2_pack(-cofs, -cofs);
-        f32x2 acc2 = f2_pack(0.0f, 0.0f);
+        f32x2 acc2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};  // two independent chains
 #pragma unroll
         for (int j = 0; j < kVecPerThread; ++j) {
           if (tid + j * kConsumerThreads < nvec) {
@@ -466,18 +472,19 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
               const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), k2, nc2));
+                acc2[e & 1] = f2_add(acc2[e & 1], f2_exp2_offset(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), k2, nc2));
             } else {
-              acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(__uint_as_float(raw[j].x), __uint_as_float(raw[j].y)),
-                                                 k2, nc2));
-              acc2 = f2_add(acc2, f2_exp2_offset(f2_pack(__uint_as_float(raw[j].z), __uint_as_float(raw[j].w)),
-                                                 k2, nc2));
+              acc2[0] = f2_add(acc2[0], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].x),
+                                                               __uint_as_float(raw[j].y)), k2, nc2));
+              acc2[1] = f2_add(acc2[1], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].z),
+                                                               __uint_as_float(raw[j].w)), k2, nc2));
             }
           }
         }
-        float a0, a1;
-        f2_unpack(acc2, a0, a1);
-        float acc = a0 + a1;
+        float a0, a1, a2, a3;
+        f2_unpack(acc2[0], a0, a1);
+        f2_unpack(acc2[1], a2, a3);
+        float acc = (a0 + a1) + (a2 + a3);
         if (has_head) acc += ex2_approx(__fmaf_rn(head_x, kscale, -cofs));
         if (has_tail) acc += ex2_approx(__fmaf_rn(tail_x, kscale, -cofs));
         sacc += acc;
@@ -547,8 +554,8 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
 }
 
 // ------------------------------------------------------------------------------------------
-// combine (grid B), mass (grid (nchunks, B)) and pick (grid B) kernels, chained behind row_stats
-// with programmatic dependent launch
+// combine (grid (chunks or 1, B)), mass (grid (chunks, B)) and pick (grid B) kernels, chained
+// behind row_stats with programmatic dependent launch
 // ------------------------------------------------------------------------------------------
 // Per-row statistics in shared memory (one entry per record row of the request).
 struct RowStatS {
@@ -853,6 +860,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   extern __shared__ __align__(16) unsigned char fin_dyn[];
   __shared__ CombineSmem sm;
   __shared__ ReqState sst;
+  __shared__ float uprime[SV_MAX_DRAFT + 1];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.y, c = blockIdx.x;
@@ -956,7 +964,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   }
   __syncthreads();
 
-  // 2. accept tests (each position independently; the first rejection is a min-reduction)
+  // 2. accept tests (each position independently; the first rejection is a min-reduction);
+  //    the draw's uniform u' is prepared for every position the draw may land on
+  for (int k = tid; k <= n && sampled; k += kCombineThreads)
+    uprime[k] = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 1u, p.round);
   for (int k = tid; k < n; k += kCombineThreads) {
     const int x = tok(k);
     bool acc;
@@ -1033,7 +1044,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
         st.cd = exp_offset(rs[Kmax + 1 + a].m, kscale);
         st.inv_sd = __frcp_rn(rs[Kmax + 1 + a].s);
       }
-      st.u = philox_uniform_f(p.seed, static_cast<uint32_t>(a), static_cast<uint32_t>(rid), 1u, p.round);
+      st.u = uprime[a];
     }
     if (c == 0) p.req[i] = st;
     sst = st;
