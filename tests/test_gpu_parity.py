@@ -115,6 +115,32 @@ def test_many_rounds_and_workspace_reuse():
     assert _status(ws) == 0
 
 
+def test_one_workspace_across_call_shapes():
+    """Calls of different sizes, dtypes and entry points share one workspace: its completion
+    counters return to zero after every call, wherever the layout puts the other regions."""
+    cases = [W.small("c3", 2), W.c3_dfly(21, B=3, K=16, V=70001), W.small("c5", 9), W.c1_greedy(4),
+             W.small("c2", 6)]
+    need = max(sv.sv_workspace_size(sv.SV_OP_VERIFY, b.B, b.Kmax, b.V,
+                                    sv.SV_BF16 if b.dtype == "bf16" else sv.SV_F32) for b in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for b in cases:
+            if b.name.startswith("c5"):
+                out = run_ragged(b, ws=ws)
+                compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+            elif not np.any(b.temperature > 0):
+                tok, alen = sv.verify_greedy(dev_rows(b.target, b.dtype), b.Kmax, draft=dev_rows(b.draft, b.dtype),
+                                             ws=ws)
+                compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy())
+            else:
+                tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, b.dtype), dev_rows(b.draft, b.dtype),
+                                                       i32(b.tokens), f32(b.temperature), b.Kmax, seed=b.seed,
+                                                       round_=b.round, request_ids=i32(b.request_ids), ws=ws)
+                compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(),
+                        b.keep_len)
+    assert _status(ws) == 0
+
+
 # ------------------------------------------------------------------------ D-cut scheduling
 
 @pytest.mark.parametrize("seed", range(6))
