@@ -25,6 +25,7 @@
 //            crossing chunk from the chunk sums, the whole CTA scans that chunk.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
     abort_flag = 0;
     fence_proxy_async_smem();
   }
-  if (!uniform) {  // every CTA computes the same table; finalize reports invalid requests
+  if (!uniform) {  // every CTA computes the same table; the combine reports invalid requests
     const int per = (B + kStatsThreads - 1) / kStatsThreads;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
     int local = 0;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
           mbar_arrive(&full_bar[stage]);
         } else {
           mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(sp.nvec) * 16u);
-          // default L2 policy: the finalize kernel re-reads the rejected rows, often from L2
+          // default L2 policy: the draw re-reads row a of each request, often from L2
           bulk_g2s(stages + stage * kStageBytes, src + static_cast<int64_t>(c0 + sp.head) * kElt,
                    static_cast<uint32_t>(sp.nvec) * 16u, &full_bar[stage]);
         }
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
   for (int64_t t = t0; t < t1; ++t) {
     if (!row_open) {
       int n;
-      if (uniform) {  // invalid temperatures give garbage statistics; finalize rejects the request
+      if (uniform) {  // invalid temperatures give garbage statistics; the combine rejects the request
         const float T = p.temperature ? __ldg(p.temperature + rr.i) : 0.0f;
         sampled = T > 0.0f;
         kscale = sampled ? kscale_of(T) : 0.0f;
@@ -1219,9 +1220,13 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   int nb = 0;  // resident CTAs per SM at this table size (the grid is persistent)
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, row_stats_kernel<DT>, kStatsThreads, dyn)) != cudaSuccess)
     return e;
+  // one contiguous task range per CTA; with a known task count (fixed-K calls) every CTA gets the
+  // same number of (row, chunk) tasks, so the grid's CTAs finish together
   const int64_t slots = static_cast<int64_t>(p.B) * p.rows_per_req * p.nchunks;
+  const int64_t tasks = p.uniform_rows > 0 ? static_cast<int64_t>(p.B) * p.uniform_rows * p.nchunks : slots;
   const int64_t cap = static_cast<int64_t>(g_num_sms) * (nb > 0 ? nb : 1);
-  const int grid = static_cast<int>(slots < cap ? slots : cap);
+  const int64_t per_cta = (tasks + cap - 1) / cap;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, (tasks + per_cta - 1) / per_cta)));
   prof_before(SV_KERNEL_ROW_STATS, stream);
   row_stats_kernel<DT><<<grid, kStatsThreads, dyn, stream>>>(p);
   prof_after(SV_KERNEL_ROW_STATS, stream);
