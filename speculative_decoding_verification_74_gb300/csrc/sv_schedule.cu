@@ -154,23 +154,27 @@ __device__ __forceinline__ int ceil_ratio_times(float r, int N) {
   return static_cast<int>((prod + ((1ull << sh) - 1)) >> sh);
 }
 
-// Candidate budgets (eq. K_rho) clipped to [B, cap], ascending, duplicates dropped (thread 0).
+// Candidate budgets (eq. K_rho) clipped to [B, cap], ascending, duplicates dropped, computed by
+// warp 0: lane r takes ratio r, the lanes sort the values with a bitonic network over shuffles,
+// and lane 0 writes the distinct ones.
 __device__ void candidates(const ScheduleParams& p, int N, int B, SchedSmem& sm) {
+  const int lane = threadIdx.x & 31;
   const int cap = p.budget > 0 ? min(p.budget, N) : N;
-  int nc = 0;
-  for (int r = 0; r < p.n_ratios; ++r) {
-    const int K = max(min(max(ceil_ratio_times(p.ratios[r], N), B), cap), B);
-    bool dup = false;
-    for (int c = 0; c < nc; ++c) dup |= sm.cand[c] == K;
-    if (dup) continue;
-    int pos = nc++;
-    while (pos > 0 && sm.cand[pos - 1] > K) {
-      sm.cand[pos] = sm.cand[pos - 1];
-      --pos;
+  int K = INT_MAX;
+  if (lane < p.n_ratios) K = max(min(max(ceil_ratio_times(p.ratios[lane], N), B), cap), B);
+#pragma unroll
+  for (int k = 2; k <= 8; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int other = __shfl_xor_sync(0xFFFFFFFFu, K, j);
+      const bool up = (lane & k) == 0, lower = (lane & j) == 0;
+      K = lower == up ? min(K, other) : max(K, other);
     }
-    sm.cand[pos] = K;
-  }
-  sm.ncand = nc;
+  const int prev = __shfl_up_sync(0xFFFFFFFFu, K, 1);
+  const bool keep = lane < 8 && K != INT_MAX && (lane == 0 || K != prev);
+  const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
+  if (keep) sm.cand[__popc(mask & ((1u << lane) - 1u))] = K;
+  if (lane == 0) sm.ncand = __popc(mask);
 }
 
 // Merge sort of the B runs of Dmax keys (request q's keys, ascending along its positions) in
@@ -209,9 +213,17 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
   __syncthreads();
   unsigned long long* src = b;
   unsigned long long* dst = a;
+  // this thread's slots (at most kMergeMaxSlots / kSchedThreads) and their runs, for every level
+  constexpr int kPer = (kMergeMaxSlots + kSchedThreads - 1) / kSchedThreads;
+  int qs[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) qs[e] = Dmax > 0 ? (tid + e * kSchedThreads) / Dmax : 0;
   for (int lvl = 1; (1 << lvl) < B; ++lvl) {
-    for (int j = tid; j < n; j += kSchedThreads) {
-      const int q = j / Dmax;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int j = tid + e * kSchedThreads;
+      if (j >= n) break;
+      const int q = qs[e];
       const int r = q >> lvl, pr = r ^ 1;
       const int rq = r << lvl, pq = pr << lvl;
       const unsigned long long x = src[j];
@@ -361,9 +373,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
     return;
   }
 
-  // 1. candidate budgets: thread 0 computes them while the others start ranking (the ranking's
-  //    barriers publish them)
-  if (tid == 0) candidates(p, M + B, B, sm);
+  // 1. candidate budgets: warp 0 computes them before it joins the ranking (whose barriers
+  //    publish them)
+  if (warp == 0) candidates(p, M + B, B, sm);
 
   // 2-5. rank the non-root slots (s desc, request asc, position asc == ascending key), then
   //      utilities, objective, chosen K

@@ -96,8 +96,11 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
 // per-request validation (every row_stats CTA computes the same info; CTA 0 reports errors)
 // ------------------------------------------------------------------------------------------
 __device__ uint16_t request_info(const VerifyParams& p, int i, uint32_t* bad_out) {
+  // every load is issued before any is used (one round trip)
   const int n = p.keep_len ? __ldg(p.keep_len + i) : p.Kmax;
   const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
+  const int ta = p.t_off ? __ldg(p.t_off + i) : 0, tb = p.t_off ? __ldg(p.t_off + i + 1) : 0;
+  const int da = p.d_off ? __ldg(p.d_off + i) : 0, dbb = p.d_off ? __ldg(p.d_off + i + 1) : 0;
   uint32_t bad = 0;
   if (n < 0 || n > p.Kmax) bad |= SV_DEV_BAD_KEEP_LEN;
   if (!(T >= 0.0f) || isinf(T)) bad |= SV_DEV_BAD_TEMPERATURE;
@@ -105,11 +108,8 @@ __device__ uint16_t request_info(const VerifyParams& p, int i, uint32_t* bad_out
   const bool need_draft = (sampled || p.tokens == nullptr) && n > 0;  // n == 0: bonus row only
   if (sampled && n > 0 && p.tokens == nullptr) bad |= SV_DEV_BAD_TOKEN;
   if (need_draft && p.draft == nullptr) bad |= SV_DEV_NO_DRAFT_ROWS;
-  if (!bad && p.t_off && (__ldg(p.t_off + i + 1) - __ldg(p.t_off + i) < n + 1 || __ldg(p.t_off + i) < 0))
-    bad |= SV_DEV_BAD_OFFSETS;
-  if (!bad && need_draft && p.d_off &&
-      (__ldg(p.d_off + i + 1) - __ldg(p.d_off + i) < n || __ldg(p.d_off + i) < 0))
-    bad |= SV_DEV_BAD_OFFSETS;
+  if (!bad && p.t_off && (tb - ta < n + 1 || ta < 0)) bad |= SV_DEV_BAD_OFFSETS;
+  if (!bad && need_draft && p.d_off && (dbb - da < n || da < 0)) bad |= SV_DEV_BAD_OFFSETS;
   *bad_out = bad;
   if (bad) return kInfoInvalid;
   return static_cast<uint16_t>(n | (need_draft ? kInfoNeedDraft : 0) | (sampled ? kInfoSampled : 0));
