@@ -231,6 +231,24 @@ class GpuWorkload:
         return self.sched_out[0].cpu().numpy()
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Seed of a rank's input sets: every rank verifies its own independent requests."""
+    return base + 7919 * rank
+
+
+def job_totals(ms: float, positions: float, dist=None, device="cpu"):
+    """Whole-job totals over the ranks: the slowest rank's time (max) and the positions all ranks
+    verified (sum).  Without a process group, the local values."""
+    if dist is None:
+        return ms, positions
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    n = torch.tensor([positions], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_74_gb300 as sv
@@ -242,12 +260,12 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     # rotating input sets: enough distinct sets that the working set exceeds L2
-    probe = make_sets(args.workload, 1, 1000 + 7919 * rank)
+    probe = make_sets(args.workload, 1, rank_seed(1000, rank))
     b0 = probe[0]["batch"]
     set_bytes = algorithmic_bytes(b0, b0.keep_len if args.workload != "c4" else np.full(b0.B, 16))
     n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))))
     n_sets = min(n_sets, 200)
-    sets = probe + make_sets(args.workload, n_sets - 1, 1001 + 7919 * rank)
+    sets = probe + make_sets(args.workload, n_sets - 1, rank_seed(1001, rank))
     gw = GpuWorkload(args.workload, sets, dev)
 
     keeps = [gw.keep_len(j) for j in range(len(gw.sets))]
@@ -299,10 +317,8 @@ def run_gpu(args, rank, world, local_rank):
     ms = ev0.elapsed_time(ev1)
     launches = sum(glaunch[j] for j in order)
     clk = clocks.stop() if clocks else None
+    ms, job_pos = job_totals(ms, tot_pos, dist, dev)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
 
     # per-kernel durations: the same K steps replayed from graphs captured with the library's
@@ -332,6 +348,8 @@ def run_gpu(args, rank, world, local_rank):
     # end to end through host buffers: H2D of the step's inputs from pinned memory, the C ABI
     # call, D2H of the emitted tokens and accepted lengths
     e2e = run_e2e(gw, warm, steps, stream)
+    e2e_ms, e2e_pos = job_totals(e2e.pop("ms"), e2e.pop("positions"), dist, dev)
+    e2e["value"] = e2e_pos / (e2e_ms * 1e-3)
 
     if rank != 0:
         if dist:
@@ -342,7 +360,7 @@ def run_gpu(args, rank, world, local_rank):
     k1_bytes = tot_bytes / steps
     achieved = k1_bytes / (k1_avg_ms * 1e-3) / 1e9
     cpu = cpu_baseline(args.workload) if world == 1 else None
-    value = world * tot_pos / (ms * 1e-3)
+    value = job_pos / (ms * 1e-3)
     line = {
         "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
         "value": value, "unit": "positions/s", "n_gpus": world, "steps": steps, "warmup": warm,
@@ -417,7 +435,7 @@ def run_e2e(gw, warm, steps, stream):
         pos = [int(np.sum(gw.keep_len(j))) for j in range(2)]
     tot = sum(pos[j % 2] for j in range(n))
     ms = ev0.elapsed_time(ev1)
-    return {"value": tot / (ms * 1e-3), "unit": "positions/s", "h2d_bytes_per_step": h2d,
+    return {"value": tot / (ms * 1e-3), "positions": tot, "ms": ms, "unit": "positions/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "wall_s": wall,
             "note": "pinned host inputs copied to the device each step, C ABI call, tokens+lengths copied back"}
 
