@@ -328,12 +328,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
     const int Dc = min(max(D, 0), Dmax);
     const float* a_row = p.alpha + static_cast<int64_t>(i) * p.alpha_stride;
     float s = 1.0f;
-    for (int k0 = 0; k0 < Dmax; k0 += 8) {
-      float a[8];
+    for (int k0 = 0; k0 < Dmax; k0 += 16) {  // 16 confidences per round trip
+      float a[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) a[u] = k0 + u < Dmax ? __ldg(a_row + k0 + u) : 0.0f;
+      for (int u = 0; u < 16; ++u) a[u] = k0 + u < Dmax ? __ldg(a_row + k0 + u) : 0.0f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int k = k0 + u + 1;
         if (k > Dmax) break;
         unsigned long long key = ~0ull;

@@ -683,74 +683,32 @@ __device__ void warp_range_sum(const char* trow, const char* drow, int c0, int l
   *sum_p = acc_p;
 }
 
-// Inverse-CDF pick inside one chunk by a whole kPickThreads CTA.  Thread t owns the contiguous
-// entries [t*per, (t+1)*per) of the chunk (per <= 32), loaded with 16-byte vectors when the layout
-// allows, every load issued before any is used.  Returns the chunk-relative index of the first
-// entry with cumsum > rem, or, if rounding keeps every partial sum at or below rem, the last entry
-// with positive weight (-1 if none).
+// Inverse-CDF pick inside one draw range by a whole kPickThreads CTA.  Thread t owns the
+// contiguous entries [t*per, (t+1)*per) of the range.  Returns the range-relative index of the
+// first entry with cumsum > rem, or, if rounding keeps every partial sum at or below rem, the last
+// entry with positive weight (-1 if none).
 template <int DT>
 __device__ int block_pick(const char* trow, const char* drow, int c0, int len, bool residual, const ReqState& st,
                           float rem, PickSmem* sm, int tid) {
-  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
-  constexpr int kVec = 16 / kElt;
-  constexpr int kMaxPer = 32;
-  constexpr int kMaxV = 4;  // bf16: 32 entries, fp32: 16 entries per thread
+  // a draw range holds at most ceil(chunk / kDrawRanges) entries: kMaxPer per thread
+  constexpr int kMaxPer = (kStageBytes / 2 / kDrawRanges + kPickThreads - 1) / kPickThreads;
   const int lane = tid & 31, warp = tid >> 5;
   const int per = (len + kPickThreads - 1) / kPickThreads;
   const int a = min(len, tid * per), b = min(len, a + per);
   const int cnt = b - a;
-  const char* tp = trow + static_cast<int64_t>(c0 + a) * kElt;
-  const char* dp = drow + static_cast<int64_t>(c0 + a) * kElt;
-  const bool vec = per % kVec == 0 && per / kVec <= kMaxV && cnt == per &&
-                   (reinterpret_cast<uintptr_t>(tp) & 15u) == 0 &&
-                   (!residual || (reinterpret_cast<uintptr_t>(dp) & 15u) == 0);
-  float w[kMaxPer];
+  // every load first (one round trip), then the weights
+  float tx[kMaxPer], dx[kMaxPer], w[kMaxPer];
 #pragma unroll
-  for (int j = 0; j < kMaxPer; ++j) w[j] = 0.0f;
-  if (vec) {
-    const int nv = per / kVec;
-    uint4 tv[kMaxV], dv[kMaxV];
+  for (int j = 0; j < kMaxPer; ++j) {
+    tx[j] = j < cnt ? load_logit<DT>(trow, c0 + a + j) : -INFINITY;
+    dx[j] = residual && j < cnt ? load_logit<DT>(drow, c0 + a + j) : -INFINITY;
+  }
 #pragma unroll
-    for (int u = 0; u < kMaxV; ++u) {
-      tv[u] = u < nv ? __ldg(reinterpret_cast<const uint4*>(tp) + u) : make_uint4(0, 0, 0, 0);
-      dv[u] = (residual && u < nv) ? __ldg(reinterpret_cast<const uint4*>(dp) + u) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kMaxV; ++u) {
-      float tx[kVec], dx[kVec];
-      if constexpr (DT == SV_BF16) {
-        const uint32_t t4[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w}, d4[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          tx[2 * e] = bf16_lo(t4[e]);
-          tx[2 * e + 1] = bf16_hi(t4[e]);
-          dx[2 * e] = bf16_lo(d4[e]);
-          dx[2 * e + 1] = bf16_hi(d4[e]);
-        }
-      } else {
-        tx[0] = __uint_as_float(tv[u].x);
-        tx[1] = __uint_as_float(tv[u].y);
-        tx[2] = __uint_as_float(tv[u].z);
-        tx[3] = __uint_as_float(tv[u].w);
-        dx[0] = __uint_as_float(dv[u].x);
-        dx[1] = __uint_as_float(dv[u].y);
-        dx[2] = __uint_as_float(dv[u].z);
-        dx[3] = __uint_as_float(dv[u].w);
-      }
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const int j = u * kVec + e;
-        if (j < kMaxPer && j < cnt) {
-          const float pv = ex2_approx(__fmaf_rn(tx[e], st.kscale, -st.ct));
-          w[j] = residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx(__fmaf_rn(dx[e], st.kscale, -st.cd)) * st.inv_sd)
-                          : pv;
-        }
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kMaxPer; ++j)
-      if (j < cnt) w[j] = draw_weight<DT>(trow, drow, c0 + a + j, residual, st);
+  for (int j = 0; j < kMaxPer; ++j) {
+    const float pv = ex2_approx(__fmaf_rn(tx[j], st.kscale, -st.ct));
+    w[j] = j >= cnt ? 0.0f
+           : residual ? fmaxf(0.0f, pv * st.inv_st - ex2_approx(__fmaf_rn(dx[j], st.kscale, -st.cd)) * st.inv_sd)
+                      : pv;
   }
   float sum = 0.0f;
   int lastpos = -1;
@@ -1103,24 +1061,25 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, NC = p.nchunks, Kmax = p.Kmax;
-  if (tid == 0) sm.st = p.req[i];
-  __syncthreads();
-  const ReqState& st = sm.st;
-  if (st.mode == kModeNone) return;
-  const bool residual_mode = st.mode == kModeResidual;
-  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
-  const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
   const int NE = NC * kDrawRanges;  // draw ranges of the request, in vocabulary order
   const float* mass_r = p.mass + static_cast<int64_t>(i) * NE;
   const float* mass_p = p.mass_p + static_cast<int64_t>(i) * NE;
   const bool staged = NE <= kPickStaged;
-  if (staged) {  // one round for every range mass of the request
+  // one round trip: the draw state and every range mass of the request (unused for requests
+  // without a draw)
+  if (tid == 0) sm.st = p.req[i];
+  if (staged) {
     for (int j = tid; j < NE; j += kPickThreads) {
       sm.mass[j] = mass_r[j];
       sm.mass[kPickStaged + j] = mass_p[j];
     }
   }
   __syncthreads();
+  const ReqState& st = sm.st;
+  if (st.mode == kModeNone) return;
+  const bool residual_mode = st.mode == kModeResidual;
+  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
+  const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
 
   // the crossing range (one warp)
   if (warp == 0) {
