@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   extern __shared__ __align__(16) unsigned char fin_dyn[];
   __shared__ CombineSmem sm;
   __shared__ ReqState sst;
-  __shared__ float uprime[SV_MAX_DRAFT + 1];
+  __shared__ float uacc[SV_MAX_DRAFT + 1], uprime[SV_MAX_DRAFT + 1];
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.y, c = blockIdx.x;
@@ -841,6 +841,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   const uint16_t info = request_info(p, i, &bad_in);
   const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
   const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
+  // the uniforms of every accept test and of the draw at every position depend only on the keys:
+  // computed while the records are in flight
+  for (int k = tid; k <= Kmax; k += kCombineThreads) {
+    uacc[k] = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 0u, p.round);
+    uprime[k] = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 1u, p.round);
+  }
   cp_async_wait_all();
   __syncthreads();
   if (c > 0 && !(info & kInfoSampled)) return;  // nothing to draw: CTA 0 does all the work
@@ -923,10 +929,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
   }
   __syncthreads();
 
-  // 2. accept tests (each position independently; the first rejection is a min-reduction);
-  //    the draw's uniform u' is prepared for every position the draw may land on
-  for (int k = tid; k <= n && sampled; k += kCombineThreads)
-    uprime[k] = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 1u, p.round);
+  // 2. accept tests (each position independently; the first rejection is a min-reduction)
   for (int k = tid; k < n; k += kCombineThreads) {
     const int x = tok(k);
     bool acc;
@@ -944,7 +947,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const VerifyPa
       // row sums are of 2^(x k - c(row max)): the drafted token's term uses the same offset
       pv = __fdiv_rn(exp2f(__fmaf_rn(rt.xval, kscale, -exp_offset(rt.m, kscale))), rt.s);
       qv = __fdiv_rn(exp2f(__fmaf_rn(rd.xval, kscale, -exp_offset(rd.m, kscale))), rd.s);
-      const float u = philox_uniform_f(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(rid), 0u, p.round);
+      const float u = uacc[k];
       acc = u * qv < pv;
       if (qv == 0.0f) atomicOr(&sm.acc_flags, SV_FLAG_Q_ZERO);
     }
