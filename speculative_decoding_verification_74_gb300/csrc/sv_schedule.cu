@@ -16,6 +16,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -429,7 +430,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const ScheduleP
   }
 }
 
-bool g_sched_attr_set = false;
+// the kernel's shared-memory attribute, set once per device under a lock
+constexpr int kMaxDevices = 64;
+bool g_sched_attr_set[kMaxDevices] = {};
+std::mutex g_sched_mu;
 
 }  // namespace
 
@@ -439,12 +443,18 @@ int launch_schedule(const ScheduleParams& p, void* stream) {
   const size_t n = static_cast<size_t>(p.B) * p.Dmax;
   const size_t dyn = (p.merge ? 2 * n : static_cast<size_t>(p.sort_size)) * 8 + n;
   cudaError_t e;
-  if (!g_sched_attr_set) {
-    const int max_dyn = SV_MAX_SCHEDULE_SLOTS * 8 + SV_MAX_SCHEDULE_SLOTS;
-    if ((e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn)) !=
-        cudaSuccess)
-      return static_cast<int>(e);
-    g_sched_attr_set = true;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return static_cast<int>(e);
+  if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+  {
+    std::lock_guard<std::mutex> lk(g_sched_mu);
+    if (!g_sched_attr_set[dev]) {
+      const int max_dyn = SV_MAX_SCHEDULE_SLOTS * 8 + SV_MAX_SCHEDULE_SLOTS;
+      if ((e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn)) !=
+          cudaSuccess)
+        return static_cast<int>(e);
+      g_sched_attr_set[dev] = true;
+    }
   }
   prof_before(SV_KERNEL_SCHEDULE, stream);
   schedule_kernel<<<1, kSchedThreads, dyn, s>>>(p);

@@ -27,6 +27,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -1133,9 +1134,40 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
   }
 }
 
-bool g_stats_attr_set[2] = {false, false};
-bool g_fin_attr_set[2] = {false, false};
-int g_num_sms = 0;
+// Per-device launch set-up, done once per device (and dtype) under a lock: function attributes
+// belong to the device that was current when they were set.
+constexpr int kMaxDevices = 64;
+struct DeviceLaunchState {
+  bool ready[2];  // attributes of the bf16 / fp32 kernels set
+  int num_sms;
+};
+DeviceLaunchState g_dev_state[kMaxDevices] = {};
+std::mutex g_dev_mu;
+
+template <int DT>
+cudaError_t device_setup(int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int di = DT == SV_BF16 ? 0 : 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceLaunchState& ds = g_dev_state[dev];
+  if (!ds.ready[di]) {
+    if (ds.num_sms == 0 && (e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    const size_t max_dyn = static_cast<size_t>(kStages) * kStageBytes + (SV_MAX_BATCH + 4) * 4 + SV_MAX_BATCH * 2;
+    if ((e = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(max_dyn))) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(combine_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kFinMaxDynSmem)) != cudaSuccess)
+      return e;
+    ds.ready[di] = true;
+  }
+  *num_sms = ds.num_sms;
+  return cudaSuccess;
+}
 
 // Launch `kernel` behind the previous kernel on the stream with programmatic dependent launch
 // (its launch overlaps the previous grid's tail; it waits in griddepcontrol.wait).  Left out
@@ -1166,19 +1198,8 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
       p.uniform_rows > 0 ? 0 : static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
   const size_t dyn = static_cast<size_t>(kStages) * kStageBytes + table;
   cudaError_t e;
-  if (g_num_sms == 0) {
-    int dev;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  }
-  const int di = DT == SV_BF16 ? 0 : 1;
-  if (!g_stats_attr_set[di]) {
-    const size_t max_dyn = static_cast<size_t>(kStages) * kStageBytes + (SV_MAX_BATCH + 4) * 4 + SV_MAX_BATCH * 2;
-    if ((e = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(max_dyn))) != cudaSuccess)
-      return e;
-    g_stats_attr_set[di] = true;
-  }
+  int num_sms = 0;
+  if ((e = device_setup<DT>(&num_sms)) != cudaSuccess) return e;
   int nb = 0;  // resident CTAs per SM at this table size (the grid is persistent)
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, row_stats_kernel<DT>, kStatsThreads, dyn)) != cudaSuccess)
     return e;
@@ -1186,7 +1207,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   // same number of (row, chunk) tasks, so the grid's CTAs finish together
   const int64_t slots = static_cast<int64_t>(p.B) * p.rows_per_req * p.nchunks;
   const int64_t tasks = p.uniform_rows > 0 ? static_cast<int64_t>(p.B) * p.uniform_rows * p.nchunks : slots;
-  const int64_t cap = static_cast<int64_t>(g_num_sms) * (nb > 0 ? nb : 1);
+  const int64_t cap = static_cast<int64_t>(num_sms) * (nb > 0 ? nb : 1);
   const int64_t per_cta = (tasks + cap - 1) / cap;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, (tasks + per_cta - 1) / per_cta)));
   prof_before(SV_KERNEL_ROW_STATS, stream);
@@ -1194,12 +1215,6 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   prof_after(SV_KERNEL_ROW_STATS, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  if (!g_fin_attr_set[di]) {
-    if ((e = cudaFuncSetAttribute(combine_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kFinMaxDynSmem)) != cudaSuccess)
-      return e;
-    g_fin_attr_set[di] = true;
-  }
   const size_t csmem = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
   if ((e = launch_pdl(combine_kernel<DT>, dim3(p.fuse_draw ? p.nchunks : 1, p.B), kCombineThreads, csmem, stream,
                       SV_KERNEL_COMBINE, p)) != cudaSuccess)
