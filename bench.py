@@ -110,20 +110,47 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons every 10 ms, with the tool's timestamps, so that the
+    samples taken inside a marked host-time window can be told apart."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.proc = None
+        self.marks = {}
         self.path = f"/tmp/sv_clocks_{os.getpid()}.csv"
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.fh,
+                                          "-lms", "10", "-i", str(gpu_index)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self, name: str):
+        self.marks[name] = time.time()
+
+    def _samples(self):
+        import datetime
+        out = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    sm, smax = float(parts[2].split()[0]), float(parts[3].split()[0])
+                except ValueError:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None  # unreadable timestamp: counted as a sample of the whole run
+                reasons = {nm for nm, v in zip(self.REASONS, parts[6:10]) if v.lower() == "active"}
+                out.append((ts, sm, smax, reasons))
+        return out
 
     def stop(self):
         if self.proc is None:
@@ -134,24 +161,27 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for ln in f:
-                parts = [x.strip() for x in ln.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1].split()[0]))
-                    smax.append(float(parts[2].split()[0]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
+        samples = self._samples()
         os.unlink(self.path)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+
+        def within(a, b):
+            if a not in self.marks or b not in self.marks:
+                return []
+            return [x for x in samples if x[0] is not None and self.marks[a] <= x[0] <= self.marks[b]]
+        timed, load = within("timed0", "timed1"), within("load0", "load1")
+        use = timed if timed else load if load else samples
+        basis = ("samples inside the timed region" if timed else
+                 "samples during a replay of the timed graphs right after the timed region (the timed region "
+                 "is shorter than the sampling interval)" if load else "all samples of the run")
+        if not timed and not load:
+            timed = samples
+        reasons = set()
+        for x in timed + load:
+            reasons |= x[3]
+        return {"sm_mhz": float(np.median([x[1] for x in use])) if use else None,
+                "sm_max_mhz": max(x[2] for x in samples) if samples else None,
+                "reasons": sorted(reasons), "samples_timed": len(timed), "samples_load": len(load),
+                "basis": basis}
 
 
 # -------------------------------------------------------------------------------- GPU arm
@@ -307,6 +337,8 @@ def run_gpu(args, rank, world, local_rank):
     time.sleep(0.3 if clocks else 0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("timed0")
     ev0.record(stream)
     for _ in range(steps // R):
         g_all.replay()
@@ -314,8 +346,18 @@ def run_gpu(args, rank, world, local_rank):
         graphs[j].replay()
     ev1.record(stream)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("timed1")
     ms = ev0.elapsed_time(ev1)
     launches = sum(glaunch[j] for j in order)
+    if clocks:  # the same graphs for ~0.3 s more, so the sampler sees the clocks under this load
+        clocks.mark("load0")
+        t_end = time.time() + 0.3
+        while time.time() < t_end:
+            for _ in range(max(1, 1000 // R)):
+                g_all.replay()
+            torch.cuda.synchronize()
+        clocks.mark("load1")
     clk = clocks.stop() if clocks else None
     ms, job_pos = job_totals(ms, tot_pos, dist, dev)
     if dist:
