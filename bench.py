@@ -169,10 +169,11 @@ class ClockSampler:
                 return []
             return [x for x in samples if x[0] is not None and self.marks[a] <= x[0] <= self.marks[b]]
         timed, load = within("timed0", "timed1"), within("load0", "load1")
-        use = timed if timed else load if load else samples
-        basis = ("samples inside the timed region" if timed else
-                 "samples during a replay of the timed graphs right after the timed region (the timed region "
-                 "is shorter than the sampling interval)" if load else "all samples of the run")
+        use = timed if len(timed) >= 3 else (timed + load) if (timed or load) else samples
+        basis = ("samples inside the timed region" if len(timed) >= 3 else
+                 "samples inside the timed region and during a replay of the timed graphs right after it (the "
+                 "timed region is short next to the 10 ms sampling interval)" if (timed or load)
+                 else "all samples of the run")
         if not timed and not load:
             timed = samples
         reasons = set()
