@@ -85,13 +85,15 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources that define the row_stats kernel and its launch (a recorded traffic
-    figure is only used while these are unchanged)."""
+    """Hash of the code that defines the row_stats kernel and its launch, with comments and
+    whitespace removed (a recorded traffic figure is only used while this code is unchanged)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_74_gb300", "csrc")
     for f in ("sv_device.cuh", "sv_internal.h", "sv_verify.cu"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            code = re.sub(r"//[^\n]*", "", fh.read())
+        h.update(f.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

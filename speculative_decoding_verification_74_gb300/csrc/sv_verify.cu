@@ -16,13 +16,14 @@
 //            L_e2e: one rejection voids every later position; AngelSpec release article, "Why
 //            one universal drafter underperforms": rejection-sampling verification in one pass).
 //            CTA 0 writes the outputs; each CTA of a short sampled request then sums its chunk of
-//            the residual max(0, p_a - q_a) after a rejection and of the target weights p_a.
-// mass       For longer requests the same chunk sums come from a separate grid (chunks, B) that
+//            the residual max(0, p_a - q_a) after a rejection and of the target weights p_a, in 8
+//            per-warp ranges.
+// mass       For longer requests the same range sums come from a separate grid (chunks, B) that
 //            reads the draw state the combine leaves.
 // pick       One CTA per request: the token at the accepted length a, drawn from
 //            norm(max(0, p_a - q_a)) after a rejection or from p_n when every drafted token was
 //            accepted (the bonus row), by inverse CDF in vocabulary order: a warp finds the
-//            crossing chunk from the chunk sums, the whole CTA scans that chunk.
+//            crossing range among the 8 x chunks range sums, the whole CTA scans that range.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -591,10 +592,10 @@ struct CombineSmem {
 struct PickSmem {
   ReqState st;
   float wsum[kPickWarps];
-  int chunk;        // crossing chunk
+  int chunk;        // crossing draw range (chunk * kDrawRanges + range)
   int bonus;        // draw from the target row (bonus, or residual mass 0)
   uint32_t flags;
-  float base;       // mass before the crossing chunk
+  float base;       // mass before the crossing range
   float thr;        // u' * Z
   int pick_thread;  // first thread whose entries hold the crossing
   int last_pos;     // broadcast of the pick
