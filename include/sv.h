@@ -135,7 +135,8 @@ sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void*
  * sampling; [explainer] "D-cut": verification stays exact).
  *
  * Per request i with temperature T = temperature[i] (device, float32):
- *   T == 0: exactly sv_verify_greedy with the given tokens (draft rows unread);
+ *   T == 0: exactly sv_verify_greedy with the given tokens (draft rows unused;
+ *           when draft is not NULL every request's draft rows are streamed);
  *           out_p = 1 if x_k is the target argmax else 0, out_q = 1.
  *   T  > 0: p_k = softmax(target_k / T), q_k = softmax(draft_k / T)
  *           accept k  <=>  u_k * q_k(x_k) < p_k(x_k),  u_k = Philox(purpose 0, k)
