@@ -20,5 +20,6 @@ enumeration, printed values), except where its docstring says
 from .philox import philox4x32_10, uniform, PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT
 from .verify import (softmax_T, verify_request, verify_batch, request_uniforms, decode_rows,
                      NEAR_ACCEPT, NEAR_PICK)
-from .schedule import prefix_confidences, k_rho, candidate_budgets, dcut_schedule
+from .schedule import (prefix_confidences, k_rho, candidate_budgets, dcut_schedule, table_cost,
+                       check_cost_table)
 from .metrics import mean_accepted_length, mean_acceptance, expected_accept_len

@@ -22,9 +22,14 @@ Readings where the pages are silent (each listed in the design notes):
     always kept: the floor K >= B in eq. K_rho reserves one slot per request.
     Remaining slots are ranked by (s descending, request ascending, position
     ascending); with 0 <= alpha <= 1 this keeps a prefix of every request.
-  * The profiled cost table is the linear model c(K) = a + b*K (float64 from
-    the float32 a, b); a budget cap clips every candidate to [B, min(budget, N)]
-    (budget <= 0 means no cap); duplicate candidates collapse.
+  * The profiled cost table is either the linear model c(K) = a + b*K
+    (float64 from the float32 a, b) or a latency table: knots (K_j, c_j) with
+    K_j strictly increasing verify-token counts and c_j > 0 the profiled
+    latencies.  Batch size and keep ratio set the token count K = K_rho(b)
+    together, so the table is read as latency against K: piecewise linear
+    between knots, the end value held outside them (table_cost).  A budget cap
+    clips every candidate to [B, min(budget, N)] (budget <= 0 means no cap);
+    duplicate candidates collapse.
   * U(K) is summed exactly as integers round(s * 2^48).
   * objective "throughput" = (U / 2^48) / c(K) (the default, "projected
     throughput"); objective "net" = U / 2^48 - c(K) ("utility minus cost").
@@ -69,10 +74,42 @@ def q48(s) -> int:
     return int(np.rint(np.float64(s) * Q48))
 
 
+def check_cost_table(knots_K, knots_c) -> tuple[list[int], list[float]]:
+    """Validate a latency table: 1..32 knots, K_j >= 1 strictly increasing, c_j finite > 0."""
+    Ks = [int(k) for k in knots_K]
+    cs = [float(c) for c in knots_c]
+    if not 1 <= len(Ks) <= 32 or len(cs) != len(Ks):
+        raise ValueError("a cost table has 1..32 knots")
+    if Ks[0] < 1 or any(b <= a for a, b in zip(Ks, Ks[1:])):
+        raise ValueError("cost-table token counts must be >= 1 and strictly increasing")
+    if not all(math.isfinite(c) and c > 0.0 for c in cs):
+        raise ValueError("cost-table latencies must be finite and positive")
+    return Ks, cs
+
+
+def table_cost(K: int, knots_K, knots_c) -> float:
+    """Latency of verifying K tokens from the profiled table (float64).
+
+    At or below the first knot: c_0; at or above the last: c_{n-1}.  Between
+    knots j and j+1: t = (K - K_j) / (K_{j+1} - K_j), then c_j + (c_{j+1} - c_j) * t,
+    each operation rounded once in that order."""
+    n = len(knots_K)
+    if K <= knots_K[0]:
+        return float(knots_c[0])
+    if K >= knots_K[n - 1]:
+        return float(knots_c[n - 1])
+    j = 0
+    while knots_K[j + 1] <= K:
+        j += 1
+    t = float(K - knots_K[j]) / float(knots_K[j + 1] - knots_K[j])
+    return float(knots_c[j]) + (float(knots_c[j + 1]) - float(knots_c[j])) * t
+
+
 def dcut_schedule(alpha, draft_len, cost_a: float, cost_b: float, budget: int,
-                  ratios=DEFAULT_RATIOS, objective: str = "throughput") -> dict:
+                  ratios=DEFAULT_RATIOS, objective: str = "throughput", cost_table=None) -> dict:
     """Return keep_len [B] (n_i), the chosen K, U(K) as an exact Q48 integer and the
-    per-candidate table."""
+    per-candidate table.  cost_table = (knots_K, knots_c) replaces the linear cost
+    a + b*K (cost_a, cost_b are then ignored)."""
     alpha = np.asarray(alpha, np.float32)
     B, Dmax = alpha.shape
     Ds = [Dmax] * B if draft_len is None else [int(v) for v in draft_len]
@@ -93,11 +130,13 @@ def dcut_schedule(alpha, draft_len, cost_a: float, cost_b: float, budget: int,
         raise ValueError("budget below one slot per request")
     a = float(np.float32(cost_a))
     b = float(np.float32(cost_b))
+    if cost_table is not None:
+        knots_K, knots_c = check_cost_table(*cost_table)
     table = []
     best = None
     for K in candidate_budgets(B, N, budget, ratios):
         U = sum(q48(e[0]) for e in order[:K])
-        cost = a + b * float(K)
+        cost = table_cost(K, knots_K, knots_c) if cost_table is not None else a + b * float(K)
         util = float(U) * (1.0 / Q48)
         obj = util / cost if objective == "throughput" else util - cost
         table.append((K, U, obj))

@@ -142,3 +142,108 @@ def test_objective_ties_pick_the_smaller_budget():
         assert len({o for _, _, o in res["table"]}) == 1
         assert res["K"] == min(K for K, _, _ in res["table"]) == 6
         assert np.all(res["keep_len"] == 0) or res["K"] > 4
+
+
+# ---- profiled latency table c(K) (AngelSpec explainer, D-cut section, Figure 3 panel 2) ----
+
+from oracle.schedule import table_cost, check_cost_table  # noqa: E402
+
+
+def _exact_interp(K, Ks, cs):
+    """Piecewise-linear interpolation in exact rationals, end values held outside."""
+    if K <= Ks[0]:
+        return Fraction(cs[0])
+    if K >= Ks[-1]:
+        return Fraction(cs[-1])
+    for j in range(len(Ks) - 1):
+        if Ks[j] <= K < Ks[j + 1]:
+            return Fraction(cs[j]) + (Fraction(cs[j + 1]) - Fraction(cs[j])) * Fraction(K - Ks[j], Ks[j + 1] - Ks[j])
+    raise AssertionError
+
+
+def _random_table(rng, lo, hi):
+    n = int(rng.integers(1, 9))
+    Ks = sorted(set(int(v) for v in rng.integers(lo, hi + 1, n)))
+    cs = [float(v) for v in rng.uniform(0.5, 40.0, len(Ks))]
+    return Ks, cs
+
+
+def test_table_cost_matches_library_interpolation():
+    """numpy.interp is piecewise-linear interpolation holding the end values outside the
+    knots; the table cost agrees with it to a few ulp of the largest latency everywhere,
+    exactly at the knots, and with the exact rational interpolant to within the four
+    roundings of its formula (each at most half an ulp of the largest latency)."""
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        Ks, cs = _random_table(rng, 1, 400)
+        for K in range(0, 420, 7):
+            got = table_cost(K, Ks, cs)
+            ref = float(np.interp(K, Ks, cs))
+            ulp = Fraction(float(np.spacing(max(cs))))
+            assert abs(Fraction(got) - Fraction(ref)) <= 8 * ulp
+            assert abs(Fraction(got) - _exact_interp(K, Ks, cs)) <= 2 * ulp
+        for k, c in zip(Ks, cs):
+            assert table_cost(k, Ks, cs) == c
+
+
+@pytest.mark.parametrize("trial", range(12))
+def test_table_cost_exhaustive_allocation_search(trial):
+    """With a latency table the chosen K maximises U(K) / c(K) (or U(K) - c(K)) computed in
+    exact rationals from the exhaustive best allocation and the exact interpolant; near-ties
+    within two roundings may go either way and are skipped."""
+    rng = np.random.default_rng(100 + trial)
+    B = int(rng.integers(1, 4))
+    Dmax = int(rng.integers(0, 4))
+    Ds = rng.integers(0, Dmax + 1, B)
+    alpha = rng.random((B, Dmax)).astype(np.float32)
+    N = int(sum(d + 1 for d in Ds))
+    Ks, cs = _random_table(rng, 1, N + 2)
+    if trial % 4 == 0:                      # knots exactly at every candidate
+        cands = candidate_budgets(B, N, 0)
+        Ks, cs = cands, [float(v) for v in rng.uniform(0.5, 5.0, len(cands))]
+    S = _scores(alpha, Ds)
+    best_by_K = {}
+    for alloc in itertools.product(*[range(D + 1) for D in Ds]):
+        K = sum(n + 1 for n in alloc)
+        best_by_K[K] = max(best_by_K.get(K, -1), sum(sum(S[i][: alloc[i] + 1]) for i in range(B)))
+    for objective in ("throughput", "net"):
+        res = dcut_schedule(alpha, Ds, 0.0, 0.0, 0, objective=objective, cost_table=(Ks, cs))
+        for K, U, _ in res["table"]:
+            assert best_by_K[K] == U
+        def obj(K):
+            u = Fraction(best_by_K[K], 2 ** 48)
+            c = _exact_interp(K, Ks, cs)
+            return u / c if objective == "throughput" else u - c
+        cands = [K for K, _, _ in res["table"]]
+        vals = sorted((obj(K) for K in cands), reverse=True)
+        if len(vals) > 1 and vals[0] != vals[1] and abs(vals[0] - vals[1]) < abs(vals[0]) * Fraction(1, 10 ** 12):
+            continue
+        top = vals[0]
+        assert res["K"] == min(K for K in cands if obj(K) == top)
+
+
+def test_table_cost_cliff_and_flat_tables():
+    """A flat table leaves utility alone to decide (the largest candidate wins when every
+    alpha > 0); a latency cliff past 300 tokens moves the C4 batch to the 272-token candidate;
+    an affine table with dyadic values reproduces the linear cost model exactly."""
+    sch = W.c4_alpha(seed=3)
+    flat = dcut_schedule(sch.alpha, sch.draft_len, 0.0, 0.0, sch.budget, cost_table=([1], [2.0]))
+    assert flat["K"] == max(K for K, _, _ in flat["table"]) == 384
+    cliff = dcut_schedule(sch.alpha, sch.draft_len, 0.0, 0.0, sch.budget,
+                          cost_table=([272, 300, 301], [10.0, 10.0, 1e6]))
+    assert cliff["K"] == 272
+    lin = dcut_schedule(sch.alpha, sch.draft_len, 1.0, 0.0625, sch.budget)
+    aff = dcut_schedule(sch.alpha, sch.draft_len, 0.0, 0.0, sch.budget,
+                        cost_table=([64, 1088], [1.0 + 0.0625 * 64, 1.0 + 0.0625 * 1088]))
+    assert [t[:2] for t in aff["table"]] == [t[:2] for t in lin["table"]]
+    assert aff["K"] == lin["K"] and np.array_equal(aff["keep_len"], lin["keep_len"])
+    assert [t[2] for t in aff["table"]] == [t[2] for t in lin["table"]]
+
+
+def test_cost_table_validation():
+    for Ks, cs in [([], []), ([0, 5], [1.0, 2.0]), ([5, 5], [1.0, 2.0]), ([5, 3], [1.0, 2.0]),
+                   ([5], [0.0]), ([5], [float("nan")]), ([5], [float("inf")]), ([1, 2], [1.0]),
+                   (list(range(1, 34)), [1.0] * 33)]:
+        with pytest.raises(ValueError):
+            check_cost_table(Ks, cs)
+    assert check_cost_table([1, 7], [0.5, 2]) == ([1, 7], [0.5, 2.0])
