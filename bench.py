@@ -282,6 +282,62 @@ def job_totals(ms: float, positions: float, dist=None, device="cpu"):
     return float(t.item()), float(n.item())
 
 
+def cost_table_leg(gw, reps: int = 200) -> dict:
+    """D-cut with a profiled latency table (c4 only, outside the timed region).
+
+    Profiles the table once, as the D-cut pipeline does at startup: the ragged verification
+    kernels of input set 0 (no target model) are timed on a (batch size x keep ratio) grid.
+    The D-cut call is then timed with the linear cost and with the table: one CUDA graph
+    each, `reps` replays between CUDA events."""
+    import torch
+    import speculative_decoding_verification_74_gb300 as sv
+    from speculative_decoding_verification_74_gb300.cost_table import profile_cost_table
+    d = gw.sets[0]
+    b, D = d["b"], gw.Kmax
+    keeps = {}
+
+    def step(nb, K):
+        if (nb, K) not in keeps:              # built on the first (untimed warm-up) call
+            extra = K - nb
+            keeps[(nb, K)] = torch.tensor([min(D, extra // nb + (1 if i < extra % nb else 0)) for i in range(nb)],
+                                          dtype=torch.int32, device=gw.dev)
+        sv.sv_verify_ragged(d["target"], b.V, d["t_off"], d["draft"], b.V, d["d_off"], d["tokens"], gw.Kmax,
+                            keeps[(nb, K)], d["temp"], b.seed, b.round, d["rid"], gw.dt, nb, gw.Kmax, gw.V,
+                            *gw.out, gw.ws, None)
+
+    grid = [16, 32, 48, 64]
+    Ks, cs = profile_cost_table(step, grid, D, reps=5, warmup=2)
+    s = d["sched"]
+    calls = {
+        "linear": lambda: sv.sv_schedule_depth(d["alpha"], gw.Kmax, None, gw.B, gw.Kmax, s.cost_a, s.cost_b,
+                                               s.budget, None, sv.SV_OBJ_THROUGHPUT, *gw.sched_out, gw.ws_sched),
+        "table": lambda: sv.sv_schedule_depth_table(d["alpha"], gw.Kmax, None, gw.B, gw.Kmax, Ks, cs, s.budget,
+                                                    None, sv.SV_OBJ_THROUGHPUT, *gw.sched_out, gw.ws_sched),
+    }
+    us, chosen = {}, {}
+    cap = torch.cuda.Stream()
+    for name, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        chosen[name] = int(gw.sched_out[2].item())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us[name] = e0.elapsed_time(e1) * 1e3 / reps
+    return {"profiled_step": "ragged verification kernels of input set 0 (no target model), median of 5",
+            "grid": {"batch_sizes": grid, "ratios": [0.25, 0.5, 0.75, 1.0], "depth": D},
+            "knots_K": Ks, "knots_ms": cs, "chosen_K": chosen,
+            "schedule_us": us, "timing": f"CUDA events over {reps} graph replays of one D-cut call"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_74_gb300 as sv
@@ -399,6 +455,8 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms, e2e_pos = job_totals(e2e.pop("ms"), e2e.pop("positions"), dist, dev)
     e2e["value"] = e2e_pos / (e2e_ms * 1e-3)
 
+    ctab = cost_table_leg(gw) if args.workload == "c4" and rank == 0 else None
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -442,6 +500,8 @@ def run_gpu(args, rank, world, local_rank):
                       "replayed K // R times, plus single-set graphs for the K % R remaining steps",
         "clocks": clk,
     }
+    if ctab is not None:
+        line["cost_table"] = ctab
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -216,6 +216,30 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
                             int64_t* out_utility_q48, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * sv_schedule_depth_table -- sv_schedule_depth with the profiled runtime latency
+ * table in place of the linear cost ([explainer] D-cut section, Figure 3 panel 2:
+ * a cost table profiled at startup across batch sizes and keep ratios picks the
+ * ratio of largest projected throughput).  Batch size and keep ratio together set
+ * the number of verified tokens K, so the table is latency against K:
+ *   cost_K [n_cost] (host): token counts, K_0 >= 1, strictly increasing
+ *   cost_c [n_cost] (host): the latency of verifying cost_K[j] tokens, finite, > 0
+ *   1 <= n_cost <= SV_MAX_COST_KNOTS; both arrays are copied at the call.
+ * c(K) = cost_c[0] for K <= cost_K[0], cost_c[n-1] for K >= cost_K[n-1], else
+ * with cost_K[j] <= K < cost_K[j+1]: t = (K - K_j) / (K_{j+1} - K_j),
+ * c = c_j + (c_{j+1} - c_j) * t, float64, each operation rounded once in that
+ * order.  Everything else (scores, ranking, candidates, U(K), both objectives,
+ * outputs, limits other than the cost, workspace) is as in sv_schedule_depth.
+ * A bad table returns SV_ERR_INVALID_ARG and enqueues nothing.
+ */
+#define SV_MAX_COST_KNOTS 32
+sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const int32_t* draft_len,
+                                  int B, int Dmax, const int32_t* cost_K, const double* cost_c,
+                                  int n_cost, int budget, const float* ratios, int n_ratios,
+                                  int objective, int32_t* out_keep_len, int32_t* out_row_offsets,
+                                  int32_t* out_total_K, int64_t* out_utility_q48, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/*
  * sv_verify_sample_noalloc -- sv_verify_sample without a caller workspace.  The AngelSpec
  * pages have no counterpart to this call; it exists for callers that cannot call cudaMalloc:
  * code that runs while its stream is being captured into a CUDA graph (an allocation there

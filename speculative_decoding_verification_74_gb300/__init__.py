@@ -48,6 +48,9 @@ _SIGS = {
                                             _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sv_schedule_depth": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _f32, _f32, _c.c_int, _vp,
                                      _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sv_schedule_depth_table": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _c.c_int,
+                                           _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz,
+                                           _vp]),
     "sv_query_status": (_c.c_int, [_vp, _vp, _c.POINTER(_u32)]),
     "sv_status_string": (_c.c_char_p, [_c.c_int]),
     "sv_last_error_string": (_c.c_char_p, []),
@@ -176,6 +179,26 @@ def sv_schedule_depth(alpha, alpha_stride, draft_len, B, Dmax, cost_a, cost_b, b
                                    _stream(stream)))
 
 
+def sv_schedule_depth_table(alpha, alpha_stride, draft_len, B, Dmax, cost_K, cost_c, budget, ratios, objective,
+                            out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, stream=None) -> None:
+    rat = None
+    n = 0
+    if ratios is not None:
+        n = len(ratios)
+        rat = (ctypes.c_float * n)(*[float(r) for r in ratios])
+    nk = len(cost_K)
+    if len(cost_c) != nk:
+        raise SVError(SV_ERR_INVALID_ARG, "cost_K and cost_c differ in length")
+    ks = (ctypes.c_int32 * max(nk, 1))(*[int(k) for k in cost_K])
+    cs = (ctypes.c_double * max(nk, 1))(*[float(c) for c in cost_c])
+    _check(lib().sv_schedule_depth_table(_p(alpha), alpha_stride, _p(draft_len), B, Dmax,
+                                         ctypes.cast(ks, ctypes.c_void_p), ctypes.cast(cs, ctypes.c_void_p), nk,
+                                         budget, ctypes.cast(rat, ctypes.c_void_p) if rat else None, n, objective,
+                                         _p(out_keep_len), _p(out_row_offsets), _p(out_total_K),
+                                         _p(out_utility_q48), _p(ws), 0 if ws is None else ws.numel(),
+                                         _stream(stream)))
+
+
 def sv_query_status(ws, stream=None) -> tuple[int, int]:
     v = ctypes.c_uint32(0)
     st = lib().sv_query_status(_p(ws), _stream(stream), ctypes.byref(v))
@@ -280,8 +303,10 @@ def verify_ragged(target, t_row_offsets, draft, d_row_offsets, draft_tokens, kee
 
 
 def schedule_depth(alpha, cost_a, cost_b, budget, *, draft_len=None, ratios=None, objective=SV_OBJ_THROUGHPUT,
-                   ws=None, stream=None, out=None):
-    """alpha [B, Dmax] float32 (device).  Returns (keep_len [B], row_offsets [B+1], total_K [1], U_q48 [1])."""
+                   ws=None, stream=None, out=None, cost_table=None):
+    """alpha [B, Dmax] float32 (device).  Returns (keep_len [B], row_offsets [B+1], total_K [1], U_q48 [1]).
+    cost_table = (token counts, latencies), e.g. from cost_table.profile_cost_table, replaces the linear
+    cost cost_a + cost_b * K (sv_schedule_depth_table)."""
     B, Dmax = alpha.shape
     dev = alpha.device
     if out is None:
@@ -289,6 +314,10 @@ def schedule_depth(alpha, cost_a, cost_b, budget, *, draft_len=None, ratios=None
                torch.empty(1, dtype=torch.int32, device=dev), torch.empty(1, dtype=torch.int64, device=dev))
     if ws is None:
         ws = workspace(SV_OP_SCHEDULE, B, Dmax, 1, SV_F32, dev)
-    sv_schedule_depth(alpha, alpha.stride(0), draft_len, B, Dmax, cost_a, cost_b, budget, ratios, objective,
-                      *out, ws, stream)
+    if cost_table is not None:
+        sv_schedule_depth_table(alpha, alpha.stride(0), draft_len, B, Dmax, cost_table[0], cost_table[1], budget,
+                                ratios, objective, *out, ws, stream)
+    else:
+        sv_schedule_depth(alpha, alpha.stride(0), draft_len, B, Dmax, cost_a, cost_b, budget, ratios, objective,
+                          *out, ws, stream)
     return out

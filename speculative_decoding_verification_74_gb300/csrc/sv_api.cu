@@ -276,10 +276,13 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
   return verify_common(p, dt, true, ws, ws_bytes, stream);
 }
 
-sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t* draft_len, int B, int Dmax,
-                            float cost_a, float cost_b, int budget, const float* ratios, int n_ratios, int objective,
-                            int32_t* out_keep_len, int32_t* out_row_offsets, int32_t* out_total_K,
-                            int64_t* out_utility_q48, void* ws, size_t ws_bytes, void* stream) {
+// Checks and launch shared by both scheduling entry points; p arrives with its cost
+// fields (cost_a, cost_b or the latency table) already set and checked.
+static sv_status schedule_common(sv::ScheduleParams& p, const float* alpha, int alpha_stride,
+                                 const int32_t* draft_len, int B, int Dmax, int budget, const float* ratios,
+                                 int n_ratios, int objective, int32_t* out_keep_len, int32_t* out_row_offsets,
+                                 int32_t* out_total_K, int64_t* out_utility_q48, void* ws, size_t ws_bytes,
+                                 void* stream) {
   if (B < 1 || B > SV_MAX_BATCH) return fail(SV_ERR_INVALID_ARG, "B=%d outside [1, %d]", B, SV_MAX_BATCH);
   if (Dmax < 0 || Dmax > SV_MAX_DRAFT) return fail(SV_ERR_INVALID_ARG, "Dmax=%d outside [0, %d]", Dmax, SV_MAX_DRAFT);
   if (static_cast<int64_t>(B) * Dmax > SV_MAX_SCHEDULE_SLOTS)
@@ -287,12 +290,9 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
   if (Dmax > 0 && (alpha == nullptr || alpha_stride < Dmax))
     return fail(SV_ERR_INVALID_ARG, "alpha is NULL or alpha_stride < Dmax");
   if (out_keep_len == nullptr || out_total_K == nullptr) return fail(SV_ERR_INVALID_ARG, "outputs are NULL");
-  if (!(cost_a >= 0.0f) || !(cost_b >= 0.0f) || !(cost_a + cost_b > 0.0f) || std::isinf(cost_a) || std::isinf(cost_b))
-    return fail(SV_ERR_INVALID_ARG, "cost model needs a >= 0, b >= 0, a + b > 0, finite");
   if (budget > 0 && budget < B) return fail(SV_ERR_INVALID_ARG, "budget %d below one slot per request (%d)", budget, B);
   if (objective != SV_OBJ_THROUGHPUT && objective != SV_OBJ_NET)
     return fail(SV_ERR_INVALID_ARG, "unknown objective %d", objective);
-  sv::ScheduleParams p = {};
   if (ratios == nullptr) {
     const float def[4] = {0.25f, 0.5f, 0.75f, 1.0f};
     p.n_ratios = 4;
@@ -314,8 +314,6 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
   p.draft_len = draft_len;
   p.B = B;
   p.Dmax = Dmax;
-  p.cost_a = static_cast<double>(cost_a);
-  p.cost_b = static_cast<double>(cost_b);
   p.budget = budget;
   p.objective = objective;
   p.sort_size = P;
@@ -328,6 +326,42 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
   const int e = sv::launch_schedule(p, stream);
   if (e != 0) return cuda_fail(e, "schedule launch");
   return SV_OK;
+}
+
+sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t* draft_len, int B, int Dmax,
+                            float cost_a, float cost_b, int budget, const float* ratios, int n_ratios, int objective,
+                            int32_t* out_keep_len, int32_t* out_row_offsets, int32_t* out_total_K,
+                            int64_t* out_utility_q48, void* ws, size_t ws_bytes, void* stream) {
+  if (!(cost_a >= 0.0f) || !(cost_b >= 0.0f) || !(cost_a + cost_b > 0.0f) || std::isinf(cost_a) || std::isinf(cost_b))
+    return fail(SV_ERR_INVALID_ARG, "cost model needs a >= 0, b >= 0, a + b > 0, finite");
+  sv::ScheduleParams p = {};
+  p.cost_a = static_cast<double>(cost_a);
+  p.cost_b = static_cast<double>(cost_b);
+  p.n_cost = 0;
+  return schedule_common(p, alpha, alpha_stride, draft_len, B, Dmax, budget, ratios, n_ratios, objective,
+                         out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, ws_bytes, stream);
+}
+
+sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const int32_t* draft_len, int B, int Dmax,
+                                  const int32_t* cost_K, const double* cost_c, int n_cost, int budget,
+                                  const float* ratios, int n_ratios, int objective, int32_t* out_keep_len,
+                                  int32_t* out_row_offsets, int32_t* out_total_K, int64_t* out_utility_q48,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (cost_K == nullptr || cost_c == nullptr) return fail(SV_ERR_INVALID_ARG, "cost table is NULL");
+  if (n_cost < 1 || n_cost > SV_MAX_COST_KNOTS)
+    return fail(SV_ERR_INVALID_ARG, "n_cost=%d outside [1, %d]", n_cost, SV_MAX_COST_KNOTS);
+  sv::ScheduleParams p = {};
+  for (int j = 0; j < n_cost; ++j) {
+    if (cost_K[j] < 1 || (j > 0 && cost_K[j] <= cost_K[j - 1]))
+      return fail(SV_ERR_INVALID_ARG, "cost_K[%d]=%d: token counts must be >= 1 and strictly increasing", j, cost_K[j]);
+    if (!(cost_c[j] > 0.0) || std::isinf(cost_c[j]))
+      return fail(SV_ERR_INVALID_ARG, "cost_c[%d] must be finite and positive", j);
+    p.cost_K[j] = cost_K[j];
+    p.cost_c[j] = cost_c[j];
+  }
+  p.n_cost = n_cost;
+  return schedule_common(p, alpha, alpha_stride, draft_len, B, Dmax, budget, ratios, n_ratios, objective,
+                         out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, ws_bytes, stream);
 }
 
 sv_status sv_query_status(void* ws, void* stream, uint32_t* device_status) {

@@ -255,6 +255,19 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
   return src;
 }
 
+// Cost of verifying K tokens (float64, explicit rounding): the linear model, or the
+// latency table interpolated linearly between knots with its end values held outside.
+__device__ double cost_of(const ScheduleParams& p, int K) {
+  if (p.n_cost == 0) return __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(K)));
+  const int n = p.n_cost;
+  if (K <= p.cost_K[0]) return p.cost_c[0];
+  if (K >= p.cost_K[n - 1]) return p.cost_c[n - 1];
+  int j = 0;  // cost_K[0] < K < cost_K[n - 1]: stops at j <= n - 2
+  while (p.cost_K[j + 1] <= K) ++j;
+  const double t = __ddiv_rn(static_cast<double>(K - p.cost_K[j]), static_cast<double>(p.cost_K[j + 1] - p.cost_K[j]));
+  return __dadd_rn(p.cost_c[j], __dmul_rn(__dsub_rn(p.cost_c[j + 1], p.cost_c[j]), t));
+}
+
 // U(K) of every candidate (exact integer sums over the first K - B sorted keys), the
 // objective, and the chosen K (same in every thread).
 __device__ void choose(const ScheduleParams& p, const unsigned long long* sorted, int n, int B, SchedSmem& sm,
@@ -287,7 +300,7 @@ __device__ void choose(const ScheduleParams& p, const unsigned long long* sorted
   if (tid < nc) {
     const long long U = sm.usum[tid] + static_cast<long long>(B) * (1ll << 48);
     const double util = __dmul_rn(__ll2double_rn(U), kTwoM48);
-    const double cost = __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(sm.cand[tid])));
+    const double cost = cost_of(p, sm.cand[tid]);
     sm.obj[tid] = p.objective == SV_OBJ_NET ? __dsub_rn(util, cost) : __ddiv_rn(util, cost);
     sm.usum[tid] = U;
   }

@@ -100,6 +100,32 @@ def test_host_validation_without_gpu(L):
                                fake, 256, None) == INV
     assert L.sv_schedule_depth(fake, 16, None, 64, 16, f(1.0), f(0.05), 0, None, 0, 0, fake, None, fake, None,
                                None, 256, None) == WS
+    # schedule with a latency table: the table's own checks, then the shared ones
+    def table(Ks, cs):
+        k = (ctypes.c_int32 * max(len(Ks), 1))(*Ks)
+        c = (ctypes.c_double * max(len(cs), 1))(*cs)
+        return ctypes.cast(k, ctypes.c_void_p), ctypes.cast(c, ctypes.c_void_p), k, c
+
+    def sched_t(Ks, cs, n=None, B=64, ws=fake, null=None):
+        k, c, _hold_k, _hold_c = table(Ks, cs)
+        if null == "K":
+            k = None
+        if null == "c":
+            c = None
+        return L.sv_schedule_depth_table(fake, 16, None, B, 16, k, c, len(Ks) if n is None else n, 0, None, 0, 0,
+                                         fake, None, fake, None, ws, 256, None)
+    assert sched_t([16, 32], [1.0, 2.0], null="K") == INV
+    assert sched_t([16, 32], [1.0, 2.0], null="c") == INV
+    assert sched_t([16, 32], [1.0, 2.0], n=0) == INV
+    assert sched_t(list(range(1, 34)), [1.0] * 33) == INV
+    assert sched_t([0, 32], [1.0, 2.0]) == INV
+    assert sched_t([32, 32], [1.0, 2.0]) == INV
+    assert sched_t([32, 16], [1.0, 2.0]) == INV
+    assert sched_t([16, 32], [1.0, 0.0]) == INV
+    assert sched_t([16, 32], [1.0, float("nan")]) == INV
+    assert sched_t([16, 32], [float("inf"), 1.0]) == INV
+    assert sched_t([16, 32], [1.0, 2.0], B=0) == INV
+    assert sched_t(list(range(1, 33)), [1.0] * 32, ws=None) == WS
     assert L.sv_query_status(None, None, None) == INV
     assert b"NULL" in L.sv_last_error_string()
 

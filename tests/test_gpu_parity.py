@@ -249,6 +249,83 @@ def test_schedule_then_ragged_verify_on_device():
     compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
 
 
+# ------------------------------------------------------------------------ D-cut with a latency table
+
+def _random_table(rng, lo, hi, n):
+    Ks = sorted(set(int(v) for v in rng.integers(lo, hi + 1, n)))
+    return Ks, [float(v) for v in rng.uniform(0.2, 50.0, len(Ks))]
+
+
+def _check_table(alpha, draft_len, budget, table, ratios=None, objective=sv.SV_OBJ_THROUGHPUT):
+    keep, offs, K, U = sv.schedule_depth(f32(alpha), 0.0, 0.0, budget, ratios=ratios, objective=objective,
+                                         draft_len=None if draft_len is None else i32(draft_len),
+                                         cost_table=table)
+    torch.cuda.synchronize()
+    o = dcut_schedule(alpha, draft_len, 0.0, 0.0, budget, ratios=ratios if ratios else (0.25, 0.5, 0.75, 1.0),
+                      objective="net" if objective == sv.SV_OBJ_NET else "throughput", cost_table=table)
+    assert int(K.item()) == o["K"] and int(U.item()) == o["U_q48"]
+    assert np.array_equal(keep.cpu().numpy(), o["keep_len"])
+    assert np.array_equal(offs.cpu().numpy(), np.concatenate([[0], np.cumsum(o["keep_len"] + 1)]))
+    return o
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_schedule_table_bit_exact(seed):
+    """Random latency tables on the D-cut batch (64 x 16): 1 to 32 knots inside, around and
+    outside the candidate range, knots exactly at the candidates, both objectives."""
+    s = W.c4_alpha(seed)
+    rng = np.random.default_rng(500 + seed)
+    N = 64 * 17
+    tables = [_random_table(rng, 64, N, n) for n in (1, 2, 5, 32)]
+    tables.append(_random_table(rng, 1, 63, 4))              # every candidate above the last knot
+    tables.append(_random_table(rng, N + 1, 4 * N, 4))       # every candidate below the first knot
+    cands = [272, 384]
+    tables.append((cands, [3.0, 4.0]))                       # knots at the candidates
+    tables.append(([272, 300, 301], [10.0, 10.0, 1e6]))      # a latency cliff past 300 tokens
+    for table in tables:
+        for objective in (sv.SV_OBJ_THROUGHPUT, sv.SV_OBJ_NET):
+            for ratios, budget in ((None, 384), ((0.1, 0.3, 0.6, 0.9, 1.0), 0)):
+                _check_table(s.alpha, None, budget, table, ratios, objective)
+    o = _check_table(s.alpha, None, 384, ([272, 300, 301], [10.0, 10.0, 1e6]))
+    assert o["K"] == 272
+
+
+def test_schedule_table_ragged_shapes():
+    for B, D in ((1, 7), (37, 20), (128, 16), (683, 3)):
+        rng = np.random.default_rng(B + D)
+        alpha = rng.beta(6, 2, (B, D)).astype(np.float32)
+        dl = rng.integers(0, D + 1, B).astype(np.int32)
+        N = int(np.sum(dl + 1))
+        for draft_len, budget in ((None, 0), (dl, max(B, N // 2))):
+            _check_table(alpha, draft_len, budget, _random_table(rng, 1, B * (D + 1), 9))
+
+
+def test_schedule_table_profiled_from_ragged_verify():
+    """Figure 3 panel 2 of the D-cut section: profile the latency table once, on a (batch size
+    x keep ratio) grid, by timing a verify step; then every step schedules with it.  The
+    profiled step here is the ragged verification itself (no target model), and the parity
+    check holds for whatever the timings come out as."""
+    from speculative_decoding_verification_74_gb300.cost_table import profile_cost_table
+    D, Bmax, V = 16, 64, 32000
+    s = W.c4_alpha(seed=11, B=Bmax, D=D)
+    b = W.c4_verify(s, np.full(Bmax, D, np.int32), seed=11, V=V)
+    target, draft = dev_rows(b.target, "bf16"), dev_rows(b.draft, "bf16")
+    t_off, d_off, toks, temp = i32(b.t_offsets), i32(b.d_offsets), i32(b.tokens), f32(b.temperature)
+    ws = sv.workspace(sv.SV_OP_VERIFY, Bmax, D, V, sv.SV_BF16)
+
+    def step(nb, K):
+        extra = K - nb                            # drafted positions spread evenly over nb requests
+        keep = np.array([min(D, extra // nb + (1 if i < extra % nb else 0)) for i in range(nb)], np.int32)
+        sv.verify_ragged(target, t_off[: nb + 1], draft, d_off[: nb + 1], toks[:nb], i32(keep), temp[:nb], D,
+                         seed=b.seed, round_=b.round, ws=ws)
+
+    Ks, cs = profile_cost_table(step, [16, 32, 64], D, reps=5, warmup=2)
+    assert Ks == sorted(set(Ks)) and all(c > 0 for c in cs) and len(Ks) <= 12
+    assert _status(ws) == 0
+    for budget in (0, 384):
+        _check_table(s.alpha, None, budget, (Ks, cs))
+
+
 # ------------------------------------------------------------------------ edge cases
 
 def test_zero_drafted_positions_and_zero_keep():
