@@ -225,9 +225,9 @@ sv_status sv_schedule_depth(const float* alpha, int alpha_stride, const int32_t*
  *   cost_c [n_cost] (host): the latency of verifying cost_K[j] tokens, finite, > 0
  *   1 <= n_cost <= SV_MAX_COST_KNOTS; both arrays are copied at the call.
  * c(K) = cost_c[0] for K <= cost_K[0], cost_c[n-1] for K >= cost_K[n-1], else
- * with cost_K[j] <= K < cost_K[j+1]: t = (K - K_j) / (K_{j+1} - K_j),
- * c = c_j + (c_{j+1} - c_j) * t, float64, each operation rounded once in that
- * order.  Everything else (scores, ranking, candidates, U(K), both objectives,
+ * with cost_K[j] <= K < cost_K[j+1], in slope form: s_j = (c_{j+1} - c_j) /
+ * (K_{j+1} - K_j) (computed on the host at the call), c = c_j + s_j * (K - K_j),
+ * float64, each operation rounded once in that order.  Everything else (scores, ranking, candidates, U(K), both objectives,
  * outputs, limits other than the cost, workspace) is as in sv_schedule_depth.
  * A bad table returns SV_ERR_INVALID_ARG and enqueues nothing.
  */

@@ -91,8 +91,9 @@ def table_cost(K: int, knots_K, knots_c) -> float:
     """Latency of verifying K tokens from the profiled table (float64).
 
     At or below the first knot: c_0; at or above the last: c_{n-1}.  Between
-    knots j and j+1: t = (K - K_j) / (K_{j+1} - K_j), then c_j + (c_{j+1} - c_j) * t,
-    each operation rounded once in that order."""
+    knots j and j+1 (K_j <= K < K_{j+1}), in slope form: the segment's slope
+    s_j = (c_{j+1} - c_j) / (K_{j+1} - K_j), then c_j + s_j * (K - K_j), each
+    operation rounded once in that order."""
     n = len(knots_K)
     if K <= knots_K[0]:
         return float(knots_c[0])
@@ -101,8 +102,8 @@ def table_cost(K: int, knots_K, knots_c) -> float:
     j = 0
     while knots_K[j + 1] <= K:
         j += 1
-    t = float(K - knots_K[j]) / float(knots_K[j + 1] - knots_K[j])
-    return float(knots_c[j]) + (float(knots_c[j + 1]) - float(knots_c[j])) * t
+    slope = (float(knots_c[j + 1]) - float(knots_c[j])) / float(knots_K[j + 1] - knots_K[j])
+    return float(knots_c[j]) + slope * float(K - knots_K[j])
 
 
 def dcut_schedule(alpha, draft_len, cost_a: float, cost_b: float, budget: int,

@@ -359,6 +359,8 @@ sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const in
     p.cost_K[j] = cost_K[j];
     p.cost_c[j] = cost_c[j];
   }
+  for (int j = 0; j + 1 < n_cost; ++j)  // segment slopes, each rounded once after one rounded difference
+    p.cost_s[j] = (p.cost_c[j + 1] - p.cost_c[j]) / static_cast<double>(p.cost_K[j + 1] - p.cost_K[j]);
   p.n_cost = n_cost;
   return schedule_common(p, alpha, alpha_stride, draft_len, B, Dmax, budget, ratios, n_ratios, objective,
                          out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, ws_bytes, stream);

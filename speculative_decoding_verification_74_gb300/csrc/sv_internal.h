@@ -85,10 +85,12 @@ struct ScheduleParams {
   const int32_t* draft_len;
   int32_t B, Dmax;
   double cost_a, cost_b;
-  // n_cost == 0: c(K) = cost_a + cost_b * K; else the latency table (cost_K, cost_c)
+  // n_cost == 0: c(K) = cost_a + cost_b * K; else the latency table (cost_K, cost_c) with
+  // the slope cost_s[j] of segment j (j <= n_cost - 2), computed on the host
   int32_t n_cost;
   int32_t cost_K[SV_MAX_COST_KNOTS];
   double cost_c[SV_MAX_COST_KNOTS];
+  double cost_s[SV_MAX_COST_KNOTS];
   int32_t budget;
   int32_t n_ratios;
   float ratios[8];

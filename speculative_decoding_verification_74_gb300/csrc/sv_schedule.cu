@@ -256,16 +256,18 @@ __device__ unsigned long long* merge_runs(unsigned long long* a, unsigned long l
 }
 
 // Cost of verifying K tokens (float64, explicit rounding): the linear model, or the
-// latency table interpolated linearly between knots with its end values held outside.
+// latency table interpolated linearly between knots (slope form) with its end values held
+// outside them.  The segment is found by an unrolled count, so the knot loads are
+// independent of each other.
 __device__ double cost_of(const ScheduleParams& p, int K) {
   if (p.n_cost == 0) return __dadd_rn(p.cost_a, __dmul_rn(p.cost_b, static_cast<double>(K)));
   const int n = p.n_cost;
   if (K <= p.cost_K[0]) return p.cost_c[0];
   if (K >= p.cost_K[n - 1]) return p.cost_c[n - 1];
-  int j = 0;  // cost_K[0] < K < cost_K[n - 1]: stops at j <= n - 2
-  while (p.cost_K[j + 1] <= K) ++j;
-  const double t = __ddiv_rn(static_cast<double>(K - p.cost_K[j]), static_cast<double>(p.cost_K[j + 1] - p.cost_K[j]));
-  return __dadd_rn(p.cost_c[j], __dmul_rn(__dsub_rn(p.cost_c[j + 1], p.cost_c[j]), t));
+  int j = 0;  // cost_K[0] < K < cost_K[n - 1]: the last j <= n - 2 with cost_K[j] <= K
+#pragma unroll
+  for (int i = 1; i < SV_MAX_COST_KNOTS - 1; ++i) j += (i < n - 1 && p.cost_K[i] <= K) ? 1 : 0;
+  return __dadd_rn(p.cost_c[j], __dmul_rn(p.cost_s[j], static_cast<double>(K - p.cost_K[j])));
 }
 
 // U(K) of every candidate (exact integer sums over the first K - B sorted keys), the
