@@ -477,8 +477,10 @@ def run_gpu(args, rank, world, local_rank):
         "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
         "value": value, "unit": "positions/s", "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if gw.dt == sv.SV_BF16 else "f32", "data": "synthetic (seeded numpy generators in synth/)",
+        "dtype": "f32", "data": "synthetic (seeded numpy generators in synth/)",
         "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload]}", "B": gw.B, "Kmax": gw.Kmax, "V": gw.V,
+                   "logits": "bf16" if gw.dt == sv.SV_BF16 else "f32",
+                   "arithmetic": "f32 (exp2, sums, probabilities); f64 for the D-cut objective",
                    "positions_per_step": tot_pos / steps, "logit_bytes_per_step": k1_bytes,
                    "l2": f"{len(gw.sets)} rotating input sets, {sum(byts) / 1e6:.0f} MB of logits read > 129 MB L2",
                    "parallelism": f"replicas x{world} (independent requests, no collective)"},
