@@ -107,6 +107,33 @@ def _p(t) -> int | None:
     return t.data_ptr()
 
 
+def _need(t, name: str, dtype, count: int = 0) -> None:
+    """Host check of one array argument before its pointer reaches the kernels: its dtype, and
+    at least `count` elements of its storage from its data pointer on (the kernels index past
+    a view's shape when a stride says so).  Raw integer pointers are the caller's affair."""
+    if t is None or isinstance(t, int):
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if count > 0:
+        avail = t.untyped_storage().nbytes() // t.element_size() - t.storage_offset()
+        if avail < count:
+            raise ValueError(f"{name} holds {avail} elements from its data pointer, the call reads {count}")
+
+
+def _logit_dtype(dt: int):
+    return {SV_BF16: torch.bfloat16, SV_F32: torch.float32}.get(dt)
+
+
+def _need_rows(t, name: str, dt: int, rows: int, stride: int, V: int) -> None:
+    """Logit rows: rows x V elements at the given row stride."""
+    _need(t, name, _logit_dtype(dt), (rows - 1) * stride + V if rows > 0 and stride >= V > 0 else 0)
+
+
+def _ws_bytes(ws) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -131,34 +158,78 @@ def sv_workspace_size(op: int, B: int, Kmax: int, V: int, dt: int) -> int:
 
 def sv_verify_greedy(target, t_row_stride, draft, d_row_stride, draft_tokens, dt, B, K, V, out_tokens,
                      out_accept_len, ws, stream=None) -> None:
+    if B > 0 and K >= 0:
+        _need_rows(target, "target", dt, B * (K + 1), t_row_stride, V)
+        _need_rows(draft, "draft", dt, B * K, d_row_stride, V)
+        _need(draft_tokens, "draft_tokens", torch.int32, B * K)
+        _need(out_tokens, "out_tokens", torch.int32, B * (K + 1))
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
     _check(lib().sv_verify_greedy(_p(target), t_row_stride, _p(draft), d_row_stride, _p(draft_tokens), dt, B,
                                   K, V, _p(out_tokens), _p(out_accept_len), _p(ws),
-                                  0 if ws is None else ws.numel(), _stream(stream)))
+                                  _ws_bytes(ws), _stream(stream)))
 
 
 def sv_verify_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round_,
                      request_ids, dt, B, K, V, out_tokens, out_accept_len, out_p, out_q, out_flags, ws,
                      stream=None) -> None:
+    if B > 0 and K >= 0:
+        _need_rows(target, "target", dt, B * (K + 1), t_row_stride, V)
+        _need_rows(draft, "draft", dt, B * K, d_row_stride, V)
+        _need(draft_tokens, "draft_tokens", torch.int32, B * K)
+        _need(temperature, "temperature", torch.float32, B)
+        _need(request_ids, "request_ids", torch.int32, B)
+        _need(out_tokens, "out_tokens", torch.int32, B * (K + 1))
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
+        _need(out_p, "out_p", torch.float32, B * K)
+        _need(out_q, "out_q", torch.float32, B * K)
+        _need(out_flags, "out_flags", torch.uint8, B)
     _check(lib().sv_verify_sample(_p(target), t_row_stride, _p(draft), d_row_stride, _p(draft_tokens),
                                   _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B, K, V,
                                   _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q), _p(out_flags),
-                                  _p(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+                                  _p(ws), _ws_bytes(ws), _stream(stream)))
 
 
 def sv_verify_ragged(target, t_row_stride, t_row_offsets, draft, d_row_stride, d_row_offsets, draft_tokens,
                      tok_stride, keep_len, temperature, seed, round_, request_ids, dt, B, Kmax, V, out_tokens,
                      out_accept_len, out_p, out_q, out_flags, ws, stream=None) -> None:
+    if B > 0 and Kmax >= 0:
+        # the packed rows' extent lives in the device offsets: only the dtype is checked here
+        _need(target, "target", _logit_dtype(dt))
+        _need(draft, "draft", _logit_dtype(dt))
+        _need(t_row_offsets, "t_row_offsets", torch.int32, B + 1)
+        _need(d_row_offsets, "d_row_offsets", torch.int32, B + 1)
+        _need(draft_tokens, "draft_tokens", torch.int32,
+              (B - 1) * tok_stride + Kmax if Kmax > 0 and tok_stride >= Kmax else 0)
+        _need(keep_len, "keep_len", torch.int32, B)
+        _need(temperature, "temperature", torch.float32, B)
+        _need(request_ids, "request_ids", torch.int32, B)
+        _need(out_tokens, "out_tokens", torch.int32, B * (Kmax + 1))
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
+        _need(out_p, "out_p", torch.float32, B * Kmax)
+        _need(out_q, "out_q", torch.float32, B * Kmax)
+        _need(out_flags, "out_flags", torch.uint8, B)
     _check(lib().sv_verify_ragged(_p(target), t_row_stride, _p(t_row_offsets), _p(draft), d_row_stride,
                                   _p(d_row_offsets), _p(draft_tokens), tok_stride, _p(keep_len),
                                   _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B, Kmax,
                                   V, _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q), _p(out_flags),
-                                  _p(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+                                  _p(ws), _ws_bytes(ws), _stream(stream)))
 
 
 def sv_verify_sample_noalloc(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round_,
                              request_ids, dt, B, K, V, out_tokens, out_accept_len, out_p, out_q, out_flags,
                              stream=None) -> None:
     """sv_verify_sample on the library's built-in scratch (no workspace argument)."""
+    if B > 0 and K >= 0:
+        _need_rows(target, "target", dt, B * (K + 1), t_row_stride, V)
+        _need_rows(draft, "draft", dt, B * K, d_row_stride, V)
+        _need(draft_tokens, "draft_tokens", torch.int32, B * K)
+        _need(temperature, "temperature", torch.float32, B)
+        _need(request_ids, "request_ids", torch.int32, B)
+        _need(out_tokens, "out_tokens", torch.int32, B * (K + 1))
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
+        _need(out_p, "out_p", torch.float32, B * K)
+        _need(out_q, "out_q", torch.float32, B * K)
+        _need(out_flags, "out_flags", torch.uint8, B)
     _check(lib().sv_verify_sample_noalloc(_p(target), t_row_stride, _p(draft), d_row_stride, _p(draft_tokens),
                                           _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B,
                                           K, V, _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q),
@@ -167,6 +238,13 @@ def sv_verify_sample_noalloc(target, t_row_stride, draft, d_row_stride, draft_to
 
 def sv_schedule_depth(alpha, alpha_stride, draft_len, B, Dmax, cost_a, cost_b, budget, ratios, objective,
                       out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, stream=None) -> None:
+    if B > 0 and Dmax >= 0:
+        _need(alpha, "alpha", torch.float32, (B - 1) * alpha_stride + Dmax if Dmax > 0 and alpha_stride >= Dmax else 0)
+        _need(draft_len, "draft_len", torch.int32, B)
+        _need(out_keep_len, "out_keep_len", torch.int32, B)
+        _need(out_row_offsets, "out_row_offsets", torch.int32, B + 1)
+        _need(out_total_K, "out_total_K", torch.int32, 1)
+        _need(out_utility_q48, "out_utility_q48", torch.int64, 1)
     rat = None
     n = 0
     if ratios is not None:
@@ -175,12 +253,19 @@ def sv_schedule_depth(alpha, alpha_stride, draft_len, B, Dmax, cost_a, cost_b, b
     _check(lib().sv_schedule_depth(_p(alpha), alpha_stride, _p(draft_len), B, Dmax, float(cost_a),
                                    float(cost_b), budget, ctypes.cast(rat, ctypes.c_void_p) if rat else None,
                                    n, objective, _p(out_keep_len), _p(out_row_offsets), _p(out_total_K),
-                                   _p(out_utility_q48), _p(ws), 0 if ws is None else ws.numel(),
+                                   _p(out_utility_q48), _p(ws), _ws_bytes(ws),
                                    _stream(stream)))
 
 
 def sv_schedule_depth_table(alpha, alpha_stride, draft_len, B, Dmax, cost_K, cost_c, budget, ratios, objective,
                             out_keep_len, out_row_offsets, out_total_K, out_utility_q48, ws, stream=None) -> None:
+    if B > 0 and Dmax >= 0:
+        _need(alpha, "alpha", torch.float32, (B - 1) * alpha_stride + Dmax if Dmax > 0 and alpha_stride >= Dmax else 0)
+        _need(draft_len, "draft_len", torch.int32, B)
+        _need(out_keep_len, "out_keep_len", torch.int32, B)
+        _need(out_row_offsets, "out_row_offsets", torch.int32, B + 1)
+        _need(out_total_K, "out_total_K", torch.int32, 1)
+        _need(out_utility_q48, "out_utility_q48", torch.int64, 1)
     rat = None
     n = 0
     if ratios is not None:
@@ -195,7 +280,7 @@ def sv_schedule_depth_table(alpha, alpha_stride, draft_len, B, Dmax, cost_K, cos
                                          ctypes.cast(ks, ctypes.c_void_p), ctypes.cast(cs, ctypes.c_void_p), nk,
                                          budget, ctypes.cast(rat, ctypes.c_void_p) if rat else None, n, objective,
                                          _p(out_keep_len), _p(out_row_offsets), _p(out_total_K),
-                                         _p(out_utility_q48), _p(ws), 0 if ws is None else ws.numel(),
+                                         _p(out_utility_q48), _p(ws), _ws_bytes(ws),
                                          _stream(stream)))
 
 
