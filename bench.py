@@ -455,7 +455,12 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms, e2e_pos = job_totals(e2e.pop("ms"), e2e.pop("positions"), dist, dev)
     e2e["value"] = e2e_pos / (e2e_ms * 1e-3)
 
-    ctab = cost_table_leg(gw) if args.workload == "c4" and rank == 0 else None
+    ctab = None
+    if args.workload == "c4" and rank == 0:
+        try:
+            ctab = cost_table_leg(gw)
+        except Exception as exc:  # context only, outside the timed region: never lose the bench line
+            ctab = {"error": f"{type(exc).__name__}: {exc}"}
 
     if rank != 0:
         if dist:
