@@ -1,10 +1,14 @@
 """Benchmark: verified draft positions/s and achieved HBM GB/s of the verification hot path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sv|reference] [--workload c1..c5]
+                  [--also c2,c4,c5]
 
 One step = one verification round (plus the D-cut schedule for c4) over one batch of synthetic
 logits already resident in HBM, through the library's C ABI.  Rotating input sets whose total
-exceeds the 129 MB L2 keep every step's logits cold in L2.  Rank 0 prints one JSON line.
+exceeds the 129 MB L2 keep every step's logits cold in L2.  Rank 0 prints one JSON line: the
+headline workload (default c3, B=64 K=16 V=151936 fp32, the largest stream) with its roofline,
+end-to-end and CPU-baseline legs, and the other workloads (--also) measured the same way under
+"other_workloads".
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
 workload (the only other place this file runs oracle code, besides the cpu_baseline leg).
@@ -338,30 +342,26 @@ def cost_table_leg(gw, reps: int = 200) -> dict:
             "schedule_us": us, "timing": f"CUDA events over {reps} graph replays of one D-cut call"}
 
 
-def run_gpu(args, rank, world, local_rank):
+def measure_workload(workload, steps, warm, rank, world, dev, dist, *, full: bool) -> dict:
+    """One workload's measurement on this rank: K timed steps (CUDA graphs, rotating input sets
+    larger than L2), per-kernel durations, and, with `full`, the end-to-end leg.  Returns the
+    fields of a bench line (whole-job values where they are reduced over ranks)."""
     import torch
     import speculative_decoding_verification_74_gb300 as sv
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
 
     # rotating input sets: enough distinct sets that the working set exceeds L2
-    probe = make_sets(args.workload, 1, rank_seed(1000, rank))
+    probe = make_sets(workload, 1, rank_seed(1000, rank))
     b0 = probe[0]["batch"]
-    set_bytes = algorithmic_bytes(b0, b0.keep_len if args.workload != "c4" else np.full(b0.B, 16))
+    set_bytes = algorithmic_bytes(b0, b0.keep_len if workload != "c4" else np.full(b0.B, 16))
     n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))))
     n_sets = min(n_sets, 200)
-    sets = probe + make_sets(args.workload, n_sets - 1, rank_seed(1001, rank))
-    gw = GpuWorkload(args.workload, sets, dev)
+    sets = probe + make_sets(workload, n_sets - 1, rank_seed(1001, rank))
+    gw = GpuWorkload(workload, sets, dev)
 
     keeps = [gw.keep_len(j) for j in range(len(gw.sets))]
     pos = [int(np.sum(k)) for k in keeps]
     trows = [int(np.sum(np.asarray(k) + 1)) for k in keeps]  # target rows verified (kept + bonus)
     byts = [algorithmic_bytes(gw.sets[j]["b"], keeps[j]) for j in range(len(gw.sets))]
-    steps, warm = args.steps, args.warmup
     R = len(gw.sets)
     order = [j % R for j in range(steps)]          # the set each timed step reads
     tot_pos = sum(pos[j] for j in order)
@@ -394,7 +394,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    clocks = ClockSampler(local_rank) if rank == 0 else None
+    clocks = ClockSampler(dev.index or 0) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -449,41 +449,29 @@ def run_gpu(args, rank, world, local_rank):
         sv.sv_profile_reset()
         del g
 
-    # end to end through host buffers: H2D of the step's inputs from pinned memory, the C ABI
-    # call, D2H of the emitted tokens and accepted lengths
-    e2e = run_e2e(gw, warm, steps, stream)
-    e2e_ms, e2e_pos = job_totals(e2e.pop("ms"), e2e.pop("positions"), dist, dev)
-    e2e["value"] = e2e_pos / (e2e_ms * 1e-3)
+    e2e = None
+    if full:
+        # end to end through host buffers: H2D of the step's inputs from pinned memory, the C ABI
+        # call, D2H of the emitted tokens and accepted lengths
+        e2e = run_e2e(gw, warm, steps, stream)
+        e2e_ms, e2e_pos = job_totals(e2e.pop("ms"), e2e.pop("positions"), dist, dev)
+        e2e["value"] = e2e_pos / (e2e_ms * 1e-3)
 
     ctab = None
-    if args.workload == "c4" and rank == 0:
+    if full and workload == "c4" and rank == 0:
         try:
             ctab = cost_table_leg(gw)
         except Exception as exc:  # context only, outside the timed region: never lose the bench line
             ctab = {"error": f"{type(exc).__name__}: {exc}"}
 
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return
     peak, peak_kind = measured_peaks()
-    k1_avg_ms = kms[sv.SV_KERNEL_ROW_STATS] / max(1, kn[sv.SV_KERNEL_ROW_STATS])
+    kid = dominant_kernel(kms)
+    k1_avg_ms = kms[kid] / max(1, kn[kid])
     k1_bytes = tot_bytes / steps
     achieved = k1_bytes / (k1_avg_ms * 1e-3) / 1e9
-    cpu = cpu_baseline(args.workload) if world == 1 else None
-    if cpu is not None:
-        cpu["cpu"] = cpu_model()
-    try:
-        cpu_all = cpu_baseline_all_cores(args.workload) if world == 1 else None
-    except Exception as exc:  # the all-core figure is context only: never lose the bench line
-        cpu_all = {"error": f"{type(exc).__name__}: {exc}"}
-    value = job_pos / (ms * 1e-3)
-    line = {
-        "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
-        "value": value, "unit": "positions/s", "n_gpus": world, "steps": steps, "warmup": warm,
-        "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded numpy generators in synth/)",
-        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload]}", "B": gw.B, "Kmax": gw.Kmax, "V": gw.V,
+    out = {
+        "value": job_pos / (ms * 1e-3), "ms_per_step": ms / steps,
+        "config": {"workload": f"{workload}: {WORKLOADS[workload]}", "B": gw.B, "Kmax": gw.Kmax, "V": gw.V,
                    "logits": "bf16" if gw.dt == sv.SV_BF16 else "f32",
                    "arithmetic": "f32 (exp2, sums, probabilities); f64 for the D-cut objective",
                    "positions_per_step": tot_pos / steps, "logit_bytes_per_step": k1_bytes,
@@ -491,24 +479,83 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (independent requests, no collective)"},
         "achieved_gbs_step": tot_bytes / (ms * 1e-3) / 1e9,
         "target_rows_per_s": job_rows / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "kernel": "row_stats", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": sv.KERNEL_NAMES[kid], "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(workload),
                      "avg_launch_us": k1_avg_ms * 1e3, "bytes_per_launch": k1_bytes,
-                     "timing": "CUDA events around each row_stats launch inside graph replays of the same K steps"},
-        "kernels_us_per_step": {sv.KERNEL_NAMES[i]: kms[i] * 1e3 / steps for i in range(sv.SV_NUM_KERNELS)
-                                if kn[i]},
-        "e2e": e2e,
-        "cpu_baseline": cpu,
-        "cpu_baseline_all_cores": cpu_all,
+                     "timing": "CUDA events on the launching stream around each launch of the kernel, inside "
+                               "graph replays of the same K steps"},
+        "kernels_us_per_step": {sv.KERNEL_NAMES[i]: kms[i] * 1e3 / steps for i in range(sv.SV_NUM_KERNELS) if kn[i]},
         "gpu_launches": launches,
-        "timed_loop": "CUDA graphs of the captured C ABI calls: one graph running every input set once, "
-                      "replayed K // R times, plus single-set graphs for the K % R remaining steps",
         "clocks": clk,
     }
+    if e2e is not None:
+        out["e2e"] = e2e
     if ctab is not None:
-        line["cost_table"] = ctab
+        out["cost_table"] = ctab
+    del graphs, g_all, gw
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def dominant_kernel(kms) -> int:
+    """The library kernel with the most time in the measured steps."""
+    return int(np.argmax(kms))
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    steps, warm = args.steps, args.warmup
+    head = measure_workload(args.workload, steps, warm, rank, world, dev, dist, full=True)
+    others = {}
+    for w in args.also:
+        if w == args.workload:
+            continue
+        m = measure_workload(w, steps, warm, rank, world, dev, dist, full=False)
+        others[w] = {k: m[k] for k in ("value", "ms_per_step", "achieved_gbs_step", "roofline",
+                                       "kernels_us_per_step", "gpu_launches", "clocks")}
+        others[w]["config"] = m["config"]
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    cpu = cpu_baseline(args.workload) if world == 1 else None
+    if cpu is not None:
+        cpu["cpu"] = cpu_model()
+    try:
+        cpu_all = cpu_baseline_all_cores(args.workload) if world == 1 else None
+    except Exception as exc:  # the all-core figure is context only: never lose the bench line
+        cpu_all = {"error": f"{type(exc).__name__}: {exc}"}
+    line = {
+        "metric": "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU",
+        "value": head["value"], "unit": "positions/s", "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded numpy generators in synth/)",
+        "config": head["config"],
+        "achieved_gbs_step": head["achieved_gbs_step"],
+        "target_rows_per_s": head["target_rows_per_s"],
+        "roofline": head["roofline"],
+        "kernels_us_per_step": head["kernels_us_per_step"],
+        "e2e": head["e2e"],
+        "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
+        "gpu_launches": head["gpu_launches"],
+        "timed_loop": "CUDA graphs of the captured C ABI calls: one graph running every input set once, "
+                      "replayed K // R times, plus single-set graphs for the K % R remaining steps",
+        "clocks": head["clocks"],
+    }
+    if "cost_table" in head:
+        line["cost_table"] = head["cost_table"]
+    if others:
+        line["other_workloads"] = others
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -565,6 +612,15 @@ def run_e2e(gw, warm, steps, stream):
 
 # -------------------------------------------------------------------------------- CPU oracle
 
+def oracle_sets(workload):
+    """Input sets for the oracle legs: the workload's own recipe and request shapes.  C3 keeps 8 of
+    its 64 requests (each request is 33 fp32 rows of 151936; the oracle only ever takes a few per
+    step, and a spawned worker per core holds its own copy)."""
+    if workload == "c3":
+        return [{"batch": W.c3_dfly(1000, B=8)}]
+    return make_sets(workload, 1, 1000)
+
+
 def oracle_step(workload, sets, j, req_slice):
     from oracle.verify import verify_batch
     from oracle.schedule import dcut_schedule
@@ -584,7 +640,7 @@ def oracle_step(workload, sets, j, req_slice):
 
 def cpu_baseline(workload, budget_s: float = 15.0):
     """The oracle, as it stands, on a bounded sample of the workload (single process)."""
-    sets = make_sets(workload, 1, 1000)
+    sets = oracle_sets(workload)
     b = sets[0]["batch"]
     t0 = time.perf_counter()
     pos = 0
@@ -621,7 +677,7 @@ _ORACLE_SETS = None
 
 def _oracle_init(workload):
     global _ORACLE_SETS
-    _ORACLE_SETS = (workload, make_sets(workload, 1, 1000))
+    _ORACLE_SETS = (workload, oracle_sets(workload))
 
 
 def _oracle_ready(_):
@@ -658,7 +714,7 @@ def cpu_baseline_all_cores(workload, budget_s: float = 10.0):
 def run_reference(args, rank):
     if rank != 0:
         return
-    sets = make_sets(args.workload, 1, 1000)
+    sets = oracle_sets(args.workload)
     b = sets[0]["batch"]
     per_step = max(1, min(b.B, 4))
     for j in range(args.warmup):
@@ -682,19 +738,35 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def check_world(gpus: int, world: int) -> None:
+    """--gpus N must match the process group the launcher made (WORLD_SIZE): one rank per GPU."""
+    if gpus != world:
+        raise SystemExit(f"bench.py: --gpus {gpus} but WORLD_SIZE={world}; for N > 1 launch one rank per GPU, "
+                         f"e.g. python -m torch.distributed.run --nproc-per-node {gpus} bench.py --gpus {gpus}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="sv", choices=["sv", "reference"])
-    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="c3", choices=sorted(WORKLOADS),
+                    help="headline workload (default c3, the largest stream)")
+    ap.add_argument("--also", default="c2,c4,c5",
+                    help="comma-separated workloads measured after the headline and reported under "
+                         "other_workloads ('' for none)")
     args = ap.parse_args()
+    args.also = [w for w in args.also.split(",") if w]
+    for w in args.also:
+        if w not in WORKLOADS:
+            raise SystemExit(f"bench.py: unknown workload {w!r} in --also")
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    check_world(args.gpus, world)
     if args.impl == "reference":
         run_reference(args, rank)
         return

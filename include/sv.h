@@ -16,9 +16,10 @@
  *           allocates device memory.  Scratch comes from a caller workspace
  *           of at least sv_workspace_size(...) bytes, 256-byte aligned, that
  *           must be zero-filled once before its first use; the library leaves
- *           it reusable (its counters return to zero at the end of every
- *           call).  One workspace must not be used by two calls that may run
- *           at the same time (different streams).
+ *           it reusable (the status word stays zero unless a kernel flags an
+ *           error, and every other region is written before it is read in
+ *           each call).  One workspace must not be used by two calls that may
+ *           run at the same time (different streams).
  * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy
  *           default stream).  All work is enqueued asynchronously; no call
  *           synchronizes, except sv_query_status and sv_profile_collect.
@@ -253,8 +254,8 @@ sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const in
  * exits.  A call whose sv_workspace_size(SV_OP_VERIFY, B, K, V, dt) exceeds it returns
  * SV_ERR_WORKSPACE (message in sv_last_error_string) and enqueues nothing.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) and caches it; make
- * that first call before any stream capture.  Each call clears the start of the array
- * (status word and draw counters) with cudaMemsetAsync on `stream`.  All calls share the one
+ * that first call before any stream capture.  Each call clears the array's status word
+ * with cudaMemsetAsync on `stream`; every other region of the array is written before it is read.  All calls share the one
  * array: calls that may overlap on the GPU (different streams of one device) race.  Nothing
  * is allocated: no cudaMalloc, cudaFree or allocating library routine.  Input errors that
  * only the kernels see are reported through out_accept_len = -1 and out_flags

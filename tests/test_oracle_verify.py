@@ -16,7 +16,7 @@ import torch
 from scipy.special import softmax as sp_softmax
 
 from oracle.verify import (decode_rows, softmax_T, verify_request, verify_batch, request_uniforms,
-                           NEAR_ACCEPT)
+                           NEAR_ACCEPT, NEAR_PICK)
 from oracle.metrics import mean_accepted_length, mean_acceptance, expected_accept_len
 from synth import workloads as W
 
@@ -239,6 +239,68 @@ def test_near_boundary_flag():
     # p/q at token 0 = 0.5 exactly; u = 0.5 + 1e-9 sits on the boundary
     r = verify_request(t, d, [0], 1.0, np.array([0.5 + 1e-9]), np.array([0.1, 0.1]))
     assert r["near"] == (NEAR_ACCEPT, 0)
+
+
+# Near-boundary inverse-CDF picks.  The rows below have cumulative draw weights known in closed
+# form, so u' can be placed a chosen distance from one bin edge.  A pick is flagged when
+# u' * Z lies within 1e-6 * Z of either edge of the picked bin (the same band, relative to
+# the accept test's 1e-6, that the design notes state for the draw).
+
+def _pick_case(t, d, x, u_acc, u_res):
+    return verify_request(np.log(np.asarray(t, float)), np.log(np.asarray(d, float)), x, 1.0,
+                          np.asarray(u_acc, float), np.asarray(u_res, float))
+
+
+@pytest.mark.parametrize("delta,flagged", [(1e-8, True), (5e-7, True), (5e-6, False), (2e-5, False)])
+@pytest.mark.parametrize("side", [+1, -1])
+def test_near_pick_band_bonus_draw(delta, flagged, side):
+    """Bonus draw (every drafted token accepted), Z = 1: bonus row p = (.1, .2, .3, .4) has the
+    inner edge c[1] = 0.3.  u' = 0.3 + delta picks entry 2 with the edge below it (c[y-1]);
+    u' = 0.3 - delta picks entry 1 with the edge above it (c[y])."""
+    t = [[0.4, 0.3, 0.2, 0.1], [0.1, 0.2, 0.3, 0.4]]
+    r = _pick_case(t, [t[0]], [0], [0.5], [0.0, 0.3 + side * delta])
+    assert r["accept_len"] == 1
+    assert r["tokens"] == [0, 2 if side > 0 else 1]
+    assert r["near"] == ((NEAR_PICK, 1) if flagged else None)
+
+
+@pytest.mark.parametrize("dist,flagged", [(1e-8, True), (1e-7, True), (5e-7, False), (5e-6, False)])
+@pytest.mark.parametrize("side", [+1, -1])
+def test_near_pick_band_residual_draw(dist, flagged, side):
+    """Residual draw after a rejection, Z = 0.2: max(0, p - q) = (0, .1, .1, 0) has the inner
+    edge c[1] = 0.1.  The band is 1e-6 * Z = 2e-7 wide here, so an absolute distance of
+    5e-7 (inside 1e-6, outside 1e-6 * Z) must not be flagged: the band scales with Z."""
+    p = [0.1, 0.3, 0.2, 0.4]
+    q = [0.3, 0.2, 0.1, 0.4]
+    Z = 0.2
+    r = _pick_case([p, [0.25] * 4], [q], [0], [0.9], [(0.1 + side * dist) / Z, 0.0])
+    assert r["accept_len"] == 0                       # 0.9 * 0.3 >= 0.1: position 0 rejects
+    assert r["tokens"] == [2 if side > 0 else 1]
+    assert r["near"] == ((NEAR_PICK, 0) if flagged else None)
+
+
+def test_near_pick_band_first_and_last_entries():
+    """Edges at the ends of the vocabulary: the first entry has no edge below it (c[-1] is not
+    consulted), and a threshold just under the total mass picks the last entry."""
+    t = [[0.4, 0.3, 0.2, 0.1], [0.1, 0.2, 0.3, 0.4]]
+    r = _pick_case(t, [t[0]], [0], [0.5], [0.0, 5e-9])        # u' Z close to c[-1] = 0 only
+    assert r["tokens"] == [0, 0] and r["near"] is None
+    r = _pick_case(t, [t[0]], [0], [0.5], [0.0, 1.0 - 5e-9])  # u' Z close to c[V-1] = Z
+    assert r["tokens"] == [0, 3] and r["near"] == (NEAR_PICK, 1)
+    r = _pick_case(t, [t[0]], [0], [0.5], [0.0, 0.1 - 5e-9])  # just below c[0]
+    assert r["tokens"] == [0, 0] and r["near"] == (NEAR_PICK, 1)
+
+
+def test_near_accept_takes_precedence_and_only_the_first_is_reported():
+    """The first near-boundary decision of a request is the one reported: a near accept test at
+    position 0 hides a near pick later in the same request."""
+    t = [[0.3, 0.7], [0.5, 0.5]]
+    d = [[0.6, 0.4]]
+    # residual (0, 0.3): u' = 1e-9 puts u' Z next to the edge c[0] = 0 of the picked entry 1
+    r = _pick_case(t, d, [0], [0.9], [1e-9, 0.0])
+    assert r["accept_len"] == 0 and r["tokens"] == [1] and r["near"] == (NEAR_PICK, 0)
+    r = _pick_case(t, d, [0], [0.5 + 1e-9], [1e-9, 0.0])   # p/q = 0.5: the accept test is near too
+    assert r["accept_len"] == 0 and r["near"] == (NEAR_ACCEPT, 0)
 
 
 def test_batch_matches_per_request_and_padding():
