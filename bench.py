@@ -89,7 +89,7 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the code that defines the row_stats kernel and its launch, with comments and
+    """Hash of the code that defines the verification kernel and its launch, with comments and
     whitespace removed (a recorded traffic figure is only used while this code is unchanged)."""
     import re
     h = hashlib.sha256()
@@ -102,8 +102,8 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per row_stats launch from a committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    """DRAM bytes per verification-kernel launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -254,9 +254,9 @@ class GpuWorkload:
                 sv.sv_schedule_depth(d["alpha"], self.Kmax, None, self.B, self.Kmax, s.cost_a, s.cost_b, s.budget,
                                      None, sv.SV_OBJ_THROUGHPUT, *self.sched_out, self.ws_sched, stream)
                 keep = self.sched_out[0]
-            sv.sv_verify_ragged(d["target"], b.V, d["t_off"], d["draft"], b.V, d["d_off"], d["tokens"], self.Kmax,
-                                keep, d["temp"], b.seed, b.round, d["rid"], self.dt, self.B, self.Kmax, self.V,
-                                *self.out, self.ws, stream)
+            sv.sv_verify_ragged(d["target"], b.V, d["t_off"], b.target.shape[0], d["draft"], b.V, d["d_off"],
+                                b.draft.shape[0], d["tokens"], self.Kmax, keep, d["temp"], b.seed, b.round, d["rid"],
+                                self.dt, self.B, self.Kmax, self.V, *self.out, self.ws, stream)
 
     def keep_len(self, j):
         """Kept positions of set j (runs the schedule once for c4)."""
@@ -305,9 +305,9 @@ def cost_table_leg(gw, reps: int = 200) -> dict:
             extra = K - nb
             keeps[(nb, K)] = torch.tensor([min(D, extra // nb + (1 if i < extra % nb else 0)) for i in range(nb)],
                                           dtype=torch.int32, device=gw.dev)
-        sv.sv_verify_ragged(d["target"], b.V, d["t_off"], d["draft"], b.V, d["d_off"], d["tokens"], gw.Kmax,
-                            keeps[(nb, K)], d["temp"], b.seed, b.round, d["rid"], gw.dt, nb, gw.Kmax, gw.V,
-                            *gw.out, gw.ws, None)
+        sv.sv_verify_ragged(d["target"], b.V, d["t_off"], b.target.shape[0], d["draft"], b.V, d["d_off"],
+                            b.draft.shape[0], d["tokens"], gw.Kmax, keeps[(nb, K)], d["temp"], b.seed, b.round,
+                            d["rid"], gw.dt, nb, gw.Kmax, gw.V, *gw.out, gw.ws, None)
 
     grid = [16, 32, 48, 64]
     Ks, cs = profile_cost_table(step, grid, D, reps=5, warmup=2)

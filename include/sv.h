@@ -15,11 +15,14 @@
  *           except `ratios` of sv_schedule_depth (host).  The library never
  *           allocates device memory.  Scratch comes from a caller workspace
  *           of at least sv_workspace_size(...) bytes, 256-byte aligned, that
- *           must be zero-filled once before its first use; the library leaves
- *           it reusable (the status word stays zero unless a kernel flags an
- *           error, and every other region is written before it is read in
- *           each call).  One workspace must not be used by two calls that may
- *           run at the same time (different streams).
+ *           must be zero-filled once before its first use.  A verification call
+ *           keeps per-request completion counters in it and returns them to
+ *           zero before it ends; every other region is written before it is
+ *           read.  So a workspace stays reusable call after call, except after
+ *           sv_query_status reports SV_ERR_TIMEOUT (counters may be left
+ *           mid-count: zero the workspace again).  One workspace must not be
+ *           used by two calls that may run at the same time (different
+ *           streams).
  * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy
  *           default stream).  All work is enqueued asynchronously; no call
  *           synchronizes, except sv_query_status and sv_profile_collect.
@@ -136,8 +139,8 @@ sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void*
  * sampling; [explainer] "D-cut": verification stays exact).
  *
  * Per request i with temperature T = temperature[i] (device, float32):
- *   T == 0: exactly sv_verify_greedy with the given tokens (draft rows unused;
- *           when draft is not NULL every request's draft rows are streamed);
+ *   T == 0: exactly sv_verify_greedy with the given tokens (its draft rows are
+ *           not read);
  *           out_p = 1 if x_k is the target argmax else 0, out_q = 1.
  *   T  > 0: p_k = softmax(target_k / T), q_k = softmax(draft_k / T)
  *           accept k  <=>  u_k * q_k(x_k) < p_k(x_k),  u_k = Philox(purpose 0, k)
@@ -169,21 +172,25 @@ sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void*
  *   target row k (0 <= k <= n_i) of request i: target + (t_row_offsets[i] + k) * t_row_stride
  *   draft  row k (0 <= k <  n_i) of request i: draft  + (d_row_offsets[i] + k) * d_row_stride
  *   drafted token k: draft_tokens[i * tok_stride + k]
- * t_row_offsets / d_row_offsets are device int32 [B+1]; the kernels check
- * t_row_offsets[i+1] - t_row_offsets[i] >= n_i + 1 and the same with n_i for
- * the draft rows of sampled requests.  d_row_offsets may be NULL when draft is
- * NULL.  Outputs are [B, Kmax+1] tokens and [B, Kmax] p/q (entries k >= n_i are
- * NaN).  draft_tokens may be NULL only if every temperature is 0 and draft is
- * given (x_k = first argmax of draft row k).
+ * t_row_offsets / d_row_offsets are device int32 [B+1]; t_rows / d_rows are the
+ * numbers of rows the target / draft arrays hold.  The kernels check, per request,
+ * t_row_offsets[i] >= 0, t_row_offsets[i+1] - t_row_offsets[i] >= n_i + 1 and
+ * t_row_offsets[i] + n_i + 1 <= t_rows, and the same with n_i draft rows for the
+ * requests that read them; a request that fails gets SV_DEV_BAD_OFFSETS and
+ * reads no row.  d_row_offsets may be NULL when draft is NULL.  Outputs are
+ * [B, Kmax+1] tokens and [B, Kmax] p/q (entries k >= n_i are NaN).  draft_tokens
+ * may be NULL only if every temperature is 0 and draft is given (x_k = first
+ * argmax of draft row k).  t_rows >= 0, d_rows >= 0 (d_rows is ignored when draft
+ * is NULL).
  */
 sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets,
-                           const void* draft, int64_t d_row_stride, const int32_t* d_row_offsets,
-                           const int32_t* draft_tokens, int tok_stride, const int32_t* keep_len,
-                           const float* temperature, uint64_t seed, uint32_t round,
-                           const int32_t* request_ids, sv_dtype dt, int B, int Kmax, int V,
-                           int32_t* out_tokens, int32_t* out_accept_len, float* out_p,
-                           float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
-                           void* stream);
+                           int64_t t_rows, const void* draft, int64_t d_row_stride,
+                           const int32_t* d_row_offsets, int64_t d_rows, const int32_t* draft_tokens,
+                           int tok_stride, const int32_t* keep_len, const float* temperature,
+                           uint64_t seed, uint32_t round, const int32_t* request_ids, sv_dtype dt,
+                           int B, int Kmax, int V, int32_t* out_tokens, int32_t* out_accept_len,
+                           float* out_p, float* out_q, uint8_t* out_flags, void* ws,
+                           size_t ws_bytes, void* stream);
 
 /*
  * sv_schedule_depth -- D-cut batch-shared verification-depth allocation
@@ -254,8 +261,9 @@ sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const in
  * exits.  A call whose sv_workspace_size(SV_OP_VERIFY, B, K, V, dt) exceeds it returns
  * SV_ERR_WORKSPACE (message in sv_last_error_string) and enqueues nothing.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) and caches it; make
- * that first call before any stream capture.  Each call clears the array's status word
- * with cudaMemsetAsync on `stream`; every other region of the array is written before it is read.  All calls share the one
+ * that first call before any stream capture.  Each call clears the array's status word and
+ * completion counters with cudaMemsetAsync on `stream`; every other region of the array is written
+ * before it is read.  All calls share the one
  * array: calls that may overlap on the GPU (different streams of one device) race.  Nothing
  * is allocated: no cudaMalloc, cudaFree or allocating library routine.  Input errors that
  * only the kernels see are reported through out_accept_len = -1 and out_flags
@@ -288,12 +296,9 @@ const char* sv_last_error_string(void);
  * brackets.  sv_launch_count returns the number of library kernel launches (or
  * captured launch nodes) since the library was loaded. */
 enum {
-  SV_KERNEL_ROW_STATS = 0, /* streaming pass over the logit rows                          */
-  SV_KERNEL_COMBINE = 1,   /* accept chain (+ per-chunk draw weights for short requests)  */
-  SV_KERNEL_SCHEDULE = 2,  /* D-cut depth allocation                                      */
-  SV_KERNEL_MASS = 3,      /* per-chunk draw weights for long requests                    */
-  SV_KERNEL_PICK = 4,      /* inverse-CDF draw                                            */
-  SV_NUM_KERNELS = 5
+  SV_KERNEL_VERIFY = 0,   /* verification: stream, accept chains and draws (one launch per call) */
+  SV_KERNEL_SCHEDULE = 1, /* D-cut depth allocation                                              */
+  SV_NUM_KERNELS = 2
 };
 void sv_profile_enable(int on);
 sv_status sv_profile_collect(double* total_ms, int64_t* launches);

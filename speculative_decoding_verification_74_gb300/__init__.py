@@ -27,8 +27,11 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, S
 SV_BF16, SV_F32 = 0, 1
 SV_OP_VERIFY, SV_OP_SCHEDULE = 0, 1
 SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
-SV_KERNEL_ROW_STATS, SV_KERNEL_COMBINE, SV_KERNEL_SCHEDULE, SV_KERNEL_MASS, SV_KERNEL_PICK, SV_NUM_KERNELS = range(6)
-KERNEL_NAMES = ("row_stats", "combine", "schedule", "mass", "pick")
+(SV_DEV_BAD_TOKEN, SV_DEV_BAD_TEMPERATURE, SV_DEV_BAD_KEEP_LEN, SV_DEV_BAD_OFFSETS, SV_DEV_NO_DRAFT_ROWS,
+ SV_DEV_BAD_ALPHA, SV_DEV_BAD_DRAFT_LEN, SV_DEV_TIMEOUT) = (1 << b for b in range(8))
+SV_FLAG_Q_ZERO, SV_FLAG_Z_ZERO, SV_FLAG_INVALID = 1, 2, 4
+SV_KERNEL_VERIFY, SV_KERNEL_SCHEDULE, SV_NUM_KERNELS = range(3)
+KERNEL_NAMES = ("verify", "schedule")
 
 _c = ctypes
 _vp, _i32, _i64, _u32, _u64, _f32, _sz = (_c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_uint64,
@@ -41,9 +44,9 @@ _SIGS = {
                                     _vp, _vp, _vp, _sz, _vp]),
     "sv_verify_sample": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _u64, _u32, _vp, _c.c_int, _c.c_int,
                                     _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "sv_verify_ragged": (_c.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _c.c_int, _vp, _vp, _u64, _u32,
-                                    _vp, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp,
-                                    _vp, _sz, _vp]),
+    "sv_verify_ragged": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _c.c_int, _vp, _vp,
+                                    _u64, _u32, _vp, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _sz, _vp]),
     "sv_verify_sample_noalloc": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _u64, _u32, _vp, _c.c_int,
                                             _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "sv_schedule_depth": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _f32, _f32, _c.c_int, _vp,
@@ -189,13 +192,14 @@ def sv_verify_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, te
                                   _p(ws), _ws_bytes(ws), _stream(stream)))
 
 
-def sv_verify_ragged(target, t_row_stride, t_row_offsets, draft, d_row_stride, d_row_offsets, draft_tokens,
-                     tok_stride, keep_len, temperature, seed, round_, request_ids, dt, B, Kmax, V, out_tokens,
-                     out_accept_len, out_p, out_q, out_flags, ws, stream=None) -> None:
+def sv_verify_ragged(target, t_row_stride, t_row_offsets, t_rows, draft, d_row_stride, d_row_offsets, d_rows,
+                     draft_tokens, tok_stride, keep_len, temperature, seed, round_, request_ids, dt, B, Kmax, V,
+                     out_tokens, out_accept_len, out_p, out_q, out_flags, ws, stream=None) -> None:
     if B > 0 and Kmax >= 0:
-        # the packed rows' extent lives in the device offsets: only the dtype is checked here
-        _need(target, "target", _logit_dtype(dt))
-        _need(draft, "draft", _logit_dtype(dt))
+        # the packed arrays hold t_rows / d_rows rows; the kernels bound every request's rows by them
+        _need_rows(target, "target", dt, t_rows, t_row_stride, V)
+        if draft is not None:
+            _need_rows(draft, "draft", dt, d_rows, d_row_stride, V)
         _need(t_row_offsets, "t_row_offsets", torch.int32, B + 1)
         _need(d_row_offsets, "d_row_offsets", torch.int32, B + 1)
         _need(draft_tokens, "draft_tokens", torch.int32,
@@ -208,8 +212,8 @@ def sv_verify_ragged(target, t_row_stride, t_row_offsets, draft, d_row_stride, d
         _need(out_p, "out_p", torch.float32, B * Kmax)
         _need(out_q, "out_q", torch.float32, B * Kmax)
         _need(out_flags, "out_flags", torch.uint8, B)
-    _check(lib().sv_verify_ragged(_p(target), t_row_stride, _p(t_row_offsets), _p(draft), d_row_stride,
-                                  _p(d_row_offsets), _p(draft_tokens), tok_stride, _p(keep_len),
+    _check(lib().sv_verify_ragged(_p(target), t_row_stride, _p(t_row_offsets), t_rows, _p(draft), d_row_stride,
+                                  _p(d_row_offsets), d_rows, _p(draft_tokens), tok_stride, _p(keep_len),
                                   _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B, Kmax,
                                   V, _p(out_tokens), _p(out_accept_len), _p(out_p), _p(out_q), _p(out_flags),
                                   _p(ws), _ws_bytes(ws), _stream(stream)))
@@ -332,6 +336,11 @@ def _rows(x: torch.Tensor):
     return x, (x.stride(-2) if x.dim() >= 2 else x.shape[-1])
 
 
+def num_rows(x: torch.Tensor) -> int:
+    """Rows of V logits in a [..., V] tensor."""
+    return x.numel() // x.shape[-1] if x.shape[-1] > 0 else 0
+
+
 def verify_greedy(target, K, *, draft=None, draft_tokens=None, ws=None, stream=None):
     """target [B*(K+1), V] (or [B, K+1, V]); draft [B*K, V] or draft_tokens [B, K]."""
     V = target.shape[-1]
@@ -382,8 +391,9 @@ def verify_ragged(target, t_row_offsets, draft, d_row_offsets, draft_tokens, kee
         ws = workspace(SV_OP_VERIFY, B, Kmax, V, dt, dev)
     ds = _rows(draft)[1] if draft is not None else V
     ts_ = draft_tokens.stride(0) if draft_tokens is not None else Kmax
-    sv_verify_ragged(target, _rows(target)[1], t_row_offsets, draft, ds, d_row_offsets, draft_tokens, ts_,
-                     keep_len, temperature, seed, round_, request_ids, dt, B, Kmax, V, *out, ws, stream)
+    sv_verify_ragged(target, _rows(target)[1], t_row_offsets, num_rows(target), draft, ds, d_row_offsets,
+                     num_rows(draft) if draft is not None else 0, draft_tokens, ts_, keep_len, temperature, seed,
+                     round_, request_ids, dt, B, Kmax, V, *out, ws, stream)
     return out
 
 

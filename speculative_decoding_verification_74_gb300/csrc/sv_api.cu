@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -68,29 +69,28 @@ cudaEvent_t take_event() {
 }
 
 // ---- shared verify entry ----------------------------------------------------------------------
-sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws, size_t ws_bytes,
-                        void* stream) {
+sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, void* ws, size_t ws_bytes, void* stream) {
   if (p.B == 0) return SV_OK;  // nothing to verify: no workspace needed, nothing enqueued
   int cl, nc;
   sv::vocab_tiling(p.V, dt, &cl, &nc);
+  // every (row, chunk) task and stream unit is counted in 32-bit integers
+  const int64_t tasks = static_cast<int64_t>(p.B) * (2 * static_cast<int64_t>(p.Kmax) + 1) * nc;
+  if (tasks > INT32_MAX) return fail(SV_ERR_INVALID_ARG, "B*(2K+1)*chunks = %lld exceeds 2^31 - 1", (long long)tasks);
   const sv::VerifyLayout L = sv::verify_layout(p.B, p.Kmax, nc);
   sv_status s = check_ws(ws, ws_bytes, L.total);
   if (s != SV_OK) return s;
   unsigned char* w = static_cast<unsigned char*>(ws);
   p.chunk_len = cl;
   p.nchunks = nc;
-  p.rows_per_req = 2 * p.Kmax + 1;
-  // Fixed-K calls need no per-request plan: every request has the same rows.
-  if (p.keep_len == nullptr && p.t_off == nullptr && p.d_off == nullptr) {
-    const bool drafts = p.temperature == nullptr ? p.tokens == nullptr : p.draft != nullptr;
-    p.uniform_rows = drafts ? 2 * p.Kmax + 1 : p.Kmax + 1;
-  }
   p.status = reinterpret_cast<uint32_t*>(w + L.status);
+  p.done = reinterpret_cast<uint32_t*>(w + L.counters);
+  p.ready = p.done + SV_MAX_BATCH;
+  p.draw_done = p.ready + SV_MAX_BATCH;
   p.req = reinterpret_cast<sv::ReqState*>(w + L.req);
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
   p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
-  const int e = sv::launch_verify(p, dt, sampled, stream);
+  const int e = sv::launch_verify(p, dt, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;
 }
@@ -169,7 +169,7 @@ void prof_after(int id, void* stream) {
 // =============================================================================================
 extern "C" {
 
-int sv_abi_version(void) { return 1; }
+int sv_abi_version(void) { return 2; }
 
 size_t sv_workspace_size(int op, int B, int Kmax, int V, sv_dtype dt) {
   if (op == SV_OP_SCHEDULE) return 256;
@@ -198,9 +198,10 @@ sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void*
   p.B = B;
   p.Kmax = K;
   p.V = V;
+  p.t_rows = p.d_rows = -1;
   p.out_tokens = out_tokens;
   p.out_accept_len = out_accept_len;
-  return verify_common(p, dt, false, ws, ws_bytes, stream);
+  return verify_common(p, dt, ws, ws_bytes, stream);
 }
 
 sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
@@ -230,15 +231,17 @@ sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void*
   p.out_p = out_p;
   p.out_q = out_q;
   p.out_flags = out_flags;
-  return verify_common(p, dt, true, ws, ws_bytes, stream);
+  p.t_rows = p.d_rows = -1;
+  return verify_common(p, dt, ws, ws_bytes, stream);
 }
 
-sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets, const void* draft,
-                           int64_t d_row_stride, const int32_t* d_row_offsets, const int32_t* draft_tokens,
-                           int tok_stride, const int32_t* keep_len, const float* temperature, uint64_t seed,
-                           uint32_t round, const int32_t* request_ids, sv_dtype dt, int B, int Kmax, int V,
-                           int32_t* out_tokens, int32_t* out_accept_len, float* out_p, float* out_q,
-                           uint8_t* out_flags, void* ws, size_t ws_bytes, void* stream) {
+sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets, int64_t t_rows,
+                           const void* draft, int64_t d_row_stride, const int32_t* d_row_offsets, int64_t d_rows,
+                           const int32_t* draft_tokens, int tok_stride, const int32_t* keep_len,
+                           const float* temperature, uint64_t seed, uint32_t round, const int32_t* request_ids,
+                           sv_dtype dt, int B, int Kmax, int V, int32_t* out_tokens, int32_t* out_accept_len,
+                           float* out_p, float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
+                           void* stream) {
   sv_status s = check_common(target, t_row_stride, draft, d_row_stride, dt, B, Kmax, V, out_tokens, out_accept_len);
   if (s != SV_OK) return s;
   if (B > 0) {
@@ -250,14 +253,18 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
       return fail(SV_ERR_INVALID_ARG, "tok_stride %d < Kmax %d", tok_stride, Kmax);
     if (draft_tokens == nullptr && draft == nullptr && Kmax > 0)
       return fail(SV_ERR_INVALID_ARG, "need draft logits or draft tokens");
+    if (t_rows < 0 || (draft != nullptr && d_rows < 0))
+      return fail(SV_ERR_INVALID_ARG, "t_rows / d_rows must be >= 0");
   }
   sv::VerifyParams p = {};
   p.target = target;
   p.t_row_stride = t_row_stride;
   p.t_off = t_row_offsets;
+  p.t_rows = t_rows;
   p.draft = draft;
   p.d_row_stride = d_row_stride;
   p.d_off = d_row_offsets;
+  p.d_rows = draft != nullptr ? d_rows : 0;
   p.tokens = draft_tokens;
   p.tok_stride = tok_stride;
   p.keep_len = keep_len;
@@ -273,7 +280,7 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
   p.out_p = out_p;
   p.out_q = out_q;
   p.out_flags = out_flags;
-  return verify_common(p, dt, true, ws, ws_bytes, stream);
+  return verify_common(p, dt, ws, ws_bytes, stream);
 }
 
 // Checks and launch shared by both scheduling entry points; p arrives with its cost

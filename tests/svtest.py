@@ -7,6 +7,7 @@ import torch
 
 import speculative_decoding_verification_74_gb300 as sv
 from oracle.verify import verify_batch, NEAR_PICK
+from synth import workloads as W
 
 P_TOL = 1e-5   # absolute tolerance on reported probabilities (the stated contract)
 
@@ -43,18 +44,50 @@ def oracle(b, keep_len=None):
                         b.round, b.request_ids, b.dtype, b.Kmax)
 
 
+NEAR_TOL = 1e-6  # the oracle's near-boundary band: |u - p/q| < 1e-6, or u' Z within 1e-6 Z of a bin edge
+
+
 def near_cap(n_requests: int) -> int:
-    """Most requests a parity comparison may excuse at a near-boundary decision: one per 32
-    requests compared, at least one.  On the parity inputs the oracle excuses about one request
-    in a hundred (mostly inverse-CDF picks on wide, flat rows)."""
+    """Most requests a comparison without its batch may excuse at a near-boundary decision: one
+    per 32 requests compared, at least one."""
     return max(1, n_requests // 32)
 
 
-def compare(orc, tok, alen, p=None, q=None, keep_len=None, temps=None, requests=None, max_near=None):
+def _decode(rows, dtype):
+    return (W.bf16_bits_to_f32(rows) if dtype == "bf16" else np.asarray(rows, np.float32)).astype(np.float64)
+
+
+def expected_excused(b, orc, idx, keep_len) -> float:
+    """Expected number of requests the oracle's near-boundary band excuses, computed without the
+    oracle's band code: a draw uniform u' lands within NEAR_TOL * Z of an edge of the bin it picks
+    with probability sum_v min(r_v / Z, 2 NEAR_TOL) (r = the weights drawn from, here from scipy's
+    softmax of the row the oracle drew from), and each accept test is near with probability at
+    most 2 NEAR_TOL.  Wide flat rows (chat rows over 151936 entries at T = 1) put several percent
+    of their draws in the band; peaked rows almost none."""
+    from scipy.special import softmax
+    lam = 0.0
+    for i in idx:
+        T = float(np.float32(b.temperature[i]))
+        a = int(orc["accept_len"][i])
+        if not T > 0.0 or a < 0:
+            continue
+        n = int(keep_len[i])
+        P = softmax(_decode(b.target[b.t_offsets[i] + a], b.dtype) / T)
+        r = P
+        if a < n:
+            r = np.maximum(0.0, P - softmax(_decode(b.draft[b.d_offsets[i] + a], b.dtype) / T))
+            if not r.sum() > 0.0:
+                r = P
+        lam += float(np.minimum(r / r.sum(), 2 * NEAR_TOL).sum()) + 2 * NEAR_TOL * (a + 1)
+    return lam
+
+
+def compare(orc, tok, alen, p=None, q=None, keep_len=None, temps=None, requests=None, max_near=None, batch=None):
     """Tokens and accepted lengths bit-exact up to the first near-boundary decision the oracle
     reports (|u - p/q| < 1e-6, or an inverse-CDF pick within 1e-6 Z of a bin edge); p, q within
-    P_TOL.  At most `max_near` requests (default near_cap of the requests compared) may stop at
-    such a decision.  Returns that number, which is also printed."""
+    P_TOL.  The number of requests that stop at such a decision is bounded: with the batch given,
+    by lam + 4 sqrt(lam) + 2 with lam = expected_excused (a Poisson tail of about 1e-4); without
+    it, by near_cap; `max_near` overrides both.  Returns that number, which is also printed."""
     B = len(alen)
     near = 0
     idx = list(range(B) if requests is None else requests)
@@ -74,7 +107,13 @@ def compare(orc, tok, alen, p=None, q=None, keep_len=None, temps=None, requests=
                 assert np.allclose(p[i, :n], orc["p"][i, :n], atol=P_TOL, rtol=0), (i, p[i, :n], orc["p"][i, :n])
                 assert np.allclose(q[i, :n], orc["q"][i, :n], atol=P_TOL, rtol=0), (i, q[i, :n], orc["q"][i, :n])
             assert np.all(np.isnan(p[i, n:])) and np.all(np.isnan(q[i, n:]))
-    cap = near_cap(len(idx)) if max_near is None else max_near
+    if max_near is not None:
+        cap = max_near
+    elif batch is not None:
+        lam = expected_excused(batch, orc, idx, batch.keep_len if keep_len is None else keep_len)
+        cap = int(lam + 4.0 * np.sqrt(lam) + 2.0)
+    else:
+        cap = near_cap(len(idx))
     print(f"parity: {len(idx)} requests compared, {near} excused at a near-boundary decision (cap {cap})")
     assert near <= cap, (near, cap)
     return near

@@ -35,7 +35,7 @@ def test_exports_every_header_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert L.sv_abi_version() == 1
+    assert L.sv_abi_version() == 2
     assert L.sv_status_string(0) == b"ok"
     assert L.sv_status_string(1) == b"invalid argument"
 
@@ -76,13 +76,17 @@ def test_host_validation_without_gpu(L):
                               None, None, fake, 1 << 20, None) == INV
     assert L.sv_verify_sample(fake, 104, fake, 104, fake, None, 0, 0, None, 0, 4, 3, 100, fake, fake, None,
                               None, None, fake, 1 << 20, None) == INV
-    # ragged: offsets required, token stride >= Kmax
-    assert L.sv_verify_ragged(fake, 104, None, fake, 104, fake, fake, 3, fake, fake, 0, 0, None, 0, 4, 3, 100,
-                              fake, fake, None, None, None, fake, 1 << 20, None) == INV
-    assert L.sv_verify_ragged(fake, 104, fake, fake, 104, None, fake, 3, fake, fake, 0, 0, None, 0, 4, 3, 100,
-                              fake, fake, None, None, None, fake, 1 << 20, None) == INV
-    assert L.sv_verify_ragged(fake, 104, fake, fake, 104, fake, fake, 2, fake, fake, 0, 0, None, 0, 4, 3, 100,
-                              fake, fake, None, None, None, fake, 1 << 20, None) == INV
+    # ragged: offsets required, token stride >= Kmax, row counts >= 0
+    assert L.sv_verify_ragged(fake, 104, None, 16, fake, 104, fake, 12, fake, 3, fake, fake, 0, 0, None, 0, 4, 3,
+                              100, fake, fake, None, None, None, fake, 1 << 20, None) == INV
+    assert L.sv_verify_ragged(fake, 104, fake, 16, fake, 104, None, 12, fake, 3, fake, fake, 0, 0, None, 0, 4, 3,
+                              100, fake, fake, None, None, None, fake, 1 << 20, None) == INV
+    assert L.sv_verify_ragged(fake, 104, fake, 16, fake, 104, fake, 12, fake, 2, fake, fake, 0, 0, None, 0, 4, 3,
+                              100, fake, fake, None, None, None, fake, 1 << 20, None) == INV
+    assert L.sv_verify_ragged(fake, 104, fake, -1, fake, 104, fake, 12, fake, 3, fake, fake, 0, 0, None, 0, 4, 3,
+                              100, fake, fake, None, None, None, fake, 1 << 20, None) == INV
+    assert L.sv_verify_ragged(fake, 104, fake, 16, fake, 104, fake, -1, fake, 3, fake, fake, 0, 0, None, 0, 4, 3,
+                              100, fake, fake, None, None, None, fake, 1 << 20, None) == INV
     # schedule: sizes, costs, budget, ratios, objective
     f = ctypes.c_float
     assert L.sv_schedule_depth(fake, 16, None, 0, 16, f(1.0), f(0.05), 0, None, 0, 0, fake, None, fake, None,

@@ -77,11 +77,12 @@ def test_ragged_checks():
     out = (torch.empty(B, Km + 1, dtype=torch.int32), torch.empty(B, dtype=torch.int32), torch.empty(B, Km),
            torch.empty(B, Km), torch.empty(B, dtype=torch.uint8))
 
-    def call(t_off=offs, tok=toks, tok_stride=Km, kl=keep, o=out):
-        sv.sv_verify_ragged(tgt, V, t_off, None, V, None, tok, tok_stride, kl, temp, 0, 0, None, sv.SV_F32, B, Km, V,
-                            *o, None)
+    def call(t_off=offs, tok=toks, tok_stride=Km, kl=keep, o=out, t_rows=B * (Km + 1)):
+        sv.sv_verify_ragged(tgt, V, t_off, t_rows, None, V, None, 0, tok, tok_stride, kl, temp, 0, 0, None, sv.SV_F32,
+                            B, Km, V, *o, None)
     _raises(call, DEVICE_MSG)
     _raises(lambda: call(t_off=offs[:B].clone()), "t_row_offsets holds")
+    _raises(lambda: call(t_rows=B * (Km + 1) + 1), "target holds")       # more rows claimed than stored
     _raises(lambda: call(t_off=offs.long()), "t_row_offsets must be torch.int32")
     _raises(lambda: call(kl=keep[:2].clone()), "keep_len holds")
     _raises(lambda: call(tok_stride=Km + 1), "draft_tokens holds")       # the last request's tokens run past

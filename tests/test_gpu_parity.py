@@ -67,7 +67,7 @@ def test_greedy_ties_break_to_lowest_index():
     tok, alen = sv.verify_greedy(tgt, K, draft_tokens=i32(tokens))
     b = W.VerifyBatch("ties", "f32", B, K, V, x, np.arange(B + 1, dtype=np.int32) * (K + 1), None, None, tokens,
                       np.full(B, K, np.int32), np.zeros(B, np.float32), 0, 0, np.arange(B, dtype=np.int32))
-    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy())
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), batch=b)
 
 
 # ------------------------------------------------------------------------ sampled verification
@@ -80,28 +80,28 @@ def test_sample_small(name, seed):
                                            f32(b.temperature), b.Kmax, seed=b.seed, round_=b.round,
                                            request_ids=i32(b.request_ids), ws=ws)
     torch.cuda.synchronize()
-    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len)
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len, batch=b)
     assert _status(ws) == 0
 
 
 @pytest.mark.parametrize("make", [lambda: W.c3_dfly(21, B=3, K=16, V=70001),     # 33 rows x 18 chunks
                                   lambda: W.c2_mtp(22, B=4, K=12, V=90001)])      # 25 rows x 11 chunks
 def test_sample_long_requests_separate_draw_weights(make):
-    """Requests with more chunk records than the combine kernel re-merges per chunk: the draw
-    weights come from the separate per-chunk kernel."""
+    """Long requests (33 rows x 18 chunks, 25 rows x 11 chunks): each request's stream spans many
+    units, and its draw spans many chunks with a ragged last chunk."""
     b = make()
     tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, b.dtype), dev_rows(b.draft, b.dtype), i32(b.tokens),
                                            f32(b.temperature), b.Kmax, seed=b.seed, round_=b.round,
                                            request_ids=i32(b.request_ids))
     torch.cuda.synchronize()
-    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len)
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len, batch=b)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2, 3])
 def test_ragged_mixed_small(seed):
     b = W.small("c5", seed)                      # mixed K in {3,16}, T in {0, 0.6, 1}, packed rows
     out = run_ragged(b)
-    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
 
 
 def test_many_rounds_and_workspace_reuse():
@@ -111,7 +111,7 @@ def test_many_rounds_and_workspace_reuse():
         if ws is None:
             ws = sv.workspace(sv.SV_OP_VERIFY, b.B, b.Kmax, b.V, sv.SV_BF16)
         out = run_ragged(b, ws=ws)
-        compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+        compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
     assert _status(ws) == 0
 
 
@@ -127,17 +127,17 @@ def test_one_workspace_across_call_shapes():
         for b in cases:
             if b.name.startswith("c5"):
                 out = run_ragged(b, ws=ws)
-                compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+                compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
             elif not np.any(b.temperature > 0):
                 tok, alen = sv.verify_greedy(dev_rows(b.target, b.dtype), b.Kmax, draft=dev_rows(b.draft, b.dtype),
                                              ws=ws)
-                compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy())
+                compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), batch=b)
             else:
                 tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, b.dtype), dev_rows(b.draft, b.dtype),
                                                        i32(b.tokens), f32(b.temperature), b.Kmax, seed=b.seed,
                                                        round_=b.round, request_ids=i32(b.request_ids), ws=ws)
                 compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(),
-                        b.keep_len)
+                        b.keep_len, batch=b)
     assert _status(ws) == 0
 
 
@@ -246,7 +246,7 @@ def test_schedule_then_ragged_verify_on_device():
                            i32(b.tokens), keep_d, f32(b.temperature), b.Kmax, seed=b.seed, round_=b.round)
     torch.cuda.synchronize()
     out = [x.cpu().numpy() for x in out]
-    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
 
 
 # ------------------------------------------------------------------------ D-cut with a latency table
@@ -333,11 +333,11 @@ def test_zero_drafted_positions_and_zero_keep():
     kl = b.keep_len.copy()
     kl[::2] = 0
     out = run_ragged(b, keep_len=kl)
-    compare(oracle(b, keep_len=kl), out[0], out[1], out[2], out[3], kl)
+    compare(oracle(b, keep_len=kl), out[0], out[1], out[2], out[3], kl, batch=b)
     b0 = W.make_batch("k0", ["chat"] * 5, [0] * 5, [1.0, 0.0, 0.6, 1.0, 1.0], 777, "bf16", 3, 0,
                       {"chat": (3.0, 1.0)})
     out = run_ragged(b0)
-    compare(oracle(b0), out[0], out[1], out[2], out[3], b0.keep_len)
+    compare(oracle(b0), out[0], out[1], out[2], out[3], b0.keep_len, batch=b0)
     assert np.all(out[1] == 0)
 
 
@@ -347,7 +347,7 @@ def test_vocab_sizes_and_tails(V):
         b = W.make_batch("v", ["chat"] * 6, [3, 1, 0, 2, 3, 3], [1.0, 0.0, 0.6, 1.0, 0.0, 2.0], V, dt, V, 0,
                          {"chat": (3.0, 1.0)})
         out = run_ragged(b)
-        compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+        compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
 
 
 def test_masked_logits():
@@ -385,7 +385,7 @@ def test_identical_rows_accept_all():
             b.tokens[i, : b.keep_len[i]] = np.argmax(t, axis=1)
     out = run_ragged(b)
     assert np.array_equal(out[1], b.keep_len)
-    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
 
 
 def test_invalid_inputs_flag_and_poison():
@@ -411,8 +411,72 @@ def test_invalid_inputs_flag_and_poison():
         assert alen[1] == -1 and np.all(tok[1] == -1)
     ok = [0, 5, 6, 7]
     bb = W.c5_mixed(seed=2, rnd=0, B=8, V=1999)
-    compare(oracle(bb), tok, alen, requests=ok)
+    compare(oracle(bb), tok, alen, requests=ok, batch=bb)
     assert sv.sv_query_status(ws)[1] == 0           # cleared by the read
+
+
+def test_ragged_row_counts_bound_every_request():
+    """The packed arrays' row counts bound the last offsets: a request whose rows would run past
+    t_rows (or d_rows) is flagged and reads nothing; the others verify as usual."""
+    b = W.c5_mixed(seed=5, rnd=0, B=6, V=3001)
+    tgt, dr = dev_rows(b.target, "bf16"), dev_rows(b.draft, "bf16")
+    args = (i32(b.tokens), b.Kmax, i32(b.keep_len), f32(b.temperature), b.seed, b.round, None, sv.SV_BF16, b.B,
+            b.Kmax, b.V)
+    last = b.B - 1
+    for short_t in (True, False):
+        if not short_t and (b.temperature[last] == 0 or b.keep_len[last] == 0):
+            continue                                  # the last request reads no draft row
+        ws = sv.workspace(sv.SV_OP_VERIFY, b.B, b.Kmax, b.V, sv.SV_BF16)
+        out = (torch.full((b.B, b.Kmax + 1), -7, dtype=torch.int32, device="cuda"),
+               torch.full((b.B,), -7, dtype=torch.int32, device="cuda"),
+               torch.empty((b.B, b.Kmax), device="cuda"), torch.empty((b.B, b.Kmax), device="cuda"),
+               torch.zeros(b.B, dtype=torch.uint8, device="cuda"))
+        t_rows = int(b.t_offsets[-1]) - (1 if short_t else 0)
+        d_rows = int(b.d_offsets[-1]) - (0 if short_t else 1)
+        sv.sv_verify_ragged(tgt, b.V, i32(b.t_offsets), t_rows, dr, b.V, i32(b.d_offsets), d_rows, *args, *out, ws)
+        st, bits = sv.sv_query_status(ws)
+        assert st == sv.SV_ERR_DEVICE_INPUT and bits == sv.SV_DEV_BAD_OFFSETS
+        tok, alen = out[0].cpu().numpy(), out[1].cpu().numpy()
+        assert alen[last] == -1 and np.all(tok[last] == -1) and out[4].cpu().numpy()[last] & sv.SV_FLAG_INVALID
+        compare(oracle(b), tok, alen, requests=list(range(b.B - 1)), batch=b)
+
+
+def test_sample_fixed_k_mixed_temperatures():
+    """A fixed-K sampled call whose batch mixes greedy (T = 0) and sampled requests: the greedy
+    ones follow the target argmax chain and do not need their draft rows."""
+    b = W.make_batch("mixT", ["chat"] * 8, [3] * 8, [1.0, 0.0, 0.6, 0.0, 1.0, 2.0, 0.0, 0.6], 20011, "bf16", 31, 2,
+                     {"chat": (3.0, 1.0)})
+    tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, "bf16"), dev_rows(b.draft, "bf16"), i32(b.tokens),
+                                           f32(b.temperature), 3, seed=b.seed, round_=b.round,
+                                           request_ids=i32(b.request_ids))
+    torch.cuda.synchronize()
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len, batch=b)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_largest_draft_length(dt):
+    """K = SV_MAX_DRAFT = 1023 drafted positions per request (2047 record rows per request)."""
+    K = 1023
+    b = W.make_batch("kmax", ["chat", "chat"], [K, K], [1.0, 0.0], 2053, dt, 41, 0, {"chat": (3.0, 0.05)})
+    out = run_ragged(b)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
+    tok, alen = sv.verify_greedy(dev_rows(b.target, dt)[: 2 * (K + 1)], K,
+                                 draft_tokens=i32(np.ascontiguousarray(b.tokens)))
+    bg = W.VerifyBatch("kmax-greedy", dt, 2, K, b.V, b.target, b.t_offsets, None, None, b.tokens, b.keep_len,
+                       np.zeros(2, np.float32), 0, 0, np.arange(2, dtype=np.int32))
+    compare(oracle(bg), tok.cpu().numpy(), alen.cpu().numpy(), batch=bg)
+
+
+def test_largest_batch():
+    """B = SV_MAX_BATCH = 4096 requests in one ragged call (the unit table at its largest)."""
+    B = 4096
+    kinds = ["chat"] * B
+    rng = np.random.default_rng(9)
+    Ks = [int(k) for k in rng.integers(0, 4, B)]
+    temps = [float(t) for t in np.asarray([0.0, 0.6, 1.0], np.float32)[rng.integers(0, 3, B)]]
+    b = W.make_batch("bmax", kinds, Ks, temps, 301, "bf16", 43, 0, {"chat": (3.0, 1.0)}, Kmax=3)
+    out = run_ragged(b)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
 
 
 def test_empty_batch_is_a_no_op():
@@ -453,16 +517,16 @@ def test_gpu_emissions_follow_the_target_distribution():
 
 
 def test_draws_over_multi_chunk_pieces():
-    """Enough (row, chunk) tasks that each row_stats CTA covers several chunks of a row; half
-    the requests have draft = target (every drafted token accepted: bonus draws), half reject
+    """Enough (row, chunk) tasks that stream units span several chunks of a row; half the
+    requests have draft = target (every drafted token accepted: bonus draws), half reject
     (residual draws)."""
     b = W.make_batch("pieces", ["chat"] * 12, [3] * 12, [1.0] * 12, 151936, "bf16", 42, 0, {"chat": (3.0, 1.0)})
     for i in range(0, b.B, 2):
         b.draft[b.d_offsets[i]: b.d_offsets[i] + 3] = b.target[b.t_offsets[i]: b.t_offsets[i] + 3]
     out = run_ragged(b)
     assert np.all(out[1][::2] == 3)
-    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len)
+    compare(oracle(b), out[0], out[1], out[2], out[3], b.keep_len, batch=b)
     tok, alen, p, q, fl = sv.verify_sample(dev_rows(b.target, "bf16"), dev_rows(b.draft, "bf16"), i32(b.tokens),
                                            f32(b.temperature), 3, seed=b.seed, round_=b.round)
     torch.cuda.synchronize()
-    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len)
+    compare(oracle(b), tok.cpu().numpy(), alen.cpu().numpy(), p.cpu().numpy(), q.cpu().numpy(), b.keep_len, batch=b)

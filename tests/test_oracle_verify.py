@@ -303,6 +303,30 @@ def test_near_accept_takes_precedence_and_only_the_first_is_reported():
     assert r["accept_len"] == 0 and r["near"] == (NEAR_ACCEPT, 0)
 
 
+def test_near_pick_rate_matches_the_band_width():
+    """On flat rows (V = 20000, sigma = 1, T = 1) nearly every entry weighs more than 2e-6, so the
+    band's measure, sum_v min(r_v / Z, 2e-6), grows in proportion to its width (about 4% of the
+    draws here).  Over 3000 uniform pairs the oracle's flag count must match that measure,
+    computed from scipy's softmax (rejections draw from max(0, p - q), acceptances from the bonus
+    row): a band twice as wide, or half as wide, fails."""
+    rng = np.random.default_rng(17)
+    V = 20000
+    t = rng.normal(0, 1, size=(2, V))
+    d = t[:1] + rng.normal(0, 0.7, size=(1, V))
+    x = int(np.argmax(d[0] + rng.gumbel(size=V)))
+    P0, Q0, P1 = sp_softmax(t[0]), sp_softmax(d[0]), sp_softmax(t[1])
+    alpha = min(1.0, P0[x] / Q0[x])
+    r = np.maximum(0.0, P0 - Q0)
+    band = lambda w: float(np.minimum(w / w.sum(), 2e-6).sum())
+    n = 3000
+    lam = n * ((1.0 - alpha) * band(r) + alpha * band(P1))
+    u = rng.random((n, 2))
+    hits = sum(verify_request(t, d, [x], 1.0, u[j, :1], np.array([u[j, 1], u[j, 1]]))["near"] is not None
+               for j in range(n))
+    assert lam > 60                                   # enough expected flags to tell widths apart
+    assert abs(hits - lam) < 4.5 * np.sqrt(lam), (hits, lam)
+
+
 def test_batch_matches_per_request_and_padding():
     b = W.small("c5", seed=3)
     res = verify_batch(b.target, b.t_offsets, b.draft, b.d_offsets, b.tokens, b.keep_len,
