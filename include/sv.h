@@ -15,14 +15,11 @@
  *           except `ratios` of sv_schedule_depth (host).  The library never
  *           allocates device memory.  Scratch comes from a caller workspace
  *           of at least sv_workspace_size(...) bytes, 256-byte aligned, that
- *           must be zero-filled once before its first use.  A verification call
- *           keeps per-request completion counters in it and returns them to
- *           zero before it ends; every other region is written before it is
- *           read.  So a workspace stays reusable call after call, except after
- *           sv_query_status reports SV_ERR_TIMEOUT (counters may be left
- *           mid-count: zero the workspace again).  One workspace must not be
- *           used by two calls that may run at the same time (different
- *           streams).
+ *           must be zero-filled once before its first use; the library leaves
+ *           it reusable (the status word stays zero unless a kernel flags an
+ *           error, and every other region is written before it is read in
+ *           each call).  One workspace must not be used by two calls that may
+ *           run at the same time (different streams).
  * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy
  *           default stream).  All work is enqueued asynchronously; no call
  *           synchronizes, except sv_query_status and sv_profile_collect.
@@ -261,9 +258,9 @@ sv_status sv_schedule_depth_table(const float* alpha, int alpha_stride, const in
  * exits.  A call whose sv_workspace_size(SV_OP_VERIFY, B, K, V, dt) exceeds it returns
  * SV_ERR_WORKSPACE (message in sv_last_error_string) and enqueues nothing.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) and caches it; make
- * that first call before any stream capture.  Each call clears the array's status word and
- * completion counters with cudaMemsetAsync on `stream`; every other region of the array is written
- * before it is read.  All calls share the one
+ * that first call before any stream capture.  Each call clears only the array's status word, with
+ * cudaMemsetAsync on `stream`; every other region of the array is written before it is read.
+ * All calls share the one
  * array: calls that may overlap on the GPU (different streams of one device) race.  Nothing
  * is allocated: no cudaMalloc, cudaFree or allocating library routine.  Input errors that
  * only the kernels see are reported through out_accept_len = -1 and out_flags
@@ -276,6 +273,17 @@ sv_status sv_verify_sample_noalloc(const void* target, int64_t t_row_stride, con
                                    const int32_t* request_ids, sv_dtype dt, int B, int K, int V,
                                    int32_t* out_tokens, int32_t* out_accept_len, float* out_p,
                                    float* out_q, uint8_t* out_flags, void* stream);
+
+/* Testing hook for the bounded waits.  The next verification call (any entry
+ * point, on any thread) runs with every wait of its streaming kernel limited to
+ * wait_limit_ms (instead of about 2 s), and the producer of that kernel's first
+ * CTA issues no copy: the CTA's consumers wait for a stage nothing fills, give
+ * up after the limit, record SV_DEV_TIMEOUT and finish the launch on what they
+ * hold (that call's outputs are meaningless).  No GPU fault is involved and no
+ * copy is in flight when the CTA exits; sv_query_status then returns
+ * SV_ERR_TIMEOUT and the workspace stays usable.  wait_limit_ms <= 0 cancels a
+ * pending request. */
+void sv_test_stall_next_verify(int wait_limit_ms);
 
 /* Synchronizes `stream`, returns the workspace's device status word in
  * *device_status (SV_DEV_* bits) and clears it.  Returns SV_OK if the word was
@@ -296,9 +304,12 @@ const char* sv_last_error_string(void);
  * brackets.  sv_launch_count returns the number of library kernel launches (or
  * captured launch nodes) since the library was loaded. */
 enum {
-  SV_KERNEL_VERIFY = 0,   /* verification: stream, accept chains and draws (one launch per call) */
-  SV_KERNEL_SCHEDULE = 1, /* D-cut depth allocation                                              */
-  SV_NUM_KERNELS = 2
+  SV_KERNEL_ROW_STATS = 0, /* streaming pass over the logit rows                          */
+  SV_KERNEL_COMBINE = 1,   /* accept chain (+ per-chunk draw weights for short requests)  */
+  SV_KERNEL_SCHEDULE = 2,  /* D-cut depth allocation                                      */
+  SV_KERNEL_MASS = 3,      /* per-chunk draw weights for long requests                    */
+  SV_KERNEL_PICK = 4,      /* inverse-CDF draw                                            */
+  SV_NUM_KERNELS = 5
 };
 void sv_profile_enable(int on);
 sv_status sv_profile_collect(double* total_ms, int64_t* launches);

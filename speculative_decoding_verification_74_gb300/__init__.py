@@ -30,8 +30,8 @@ SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
 (SV_DEV_BAD_TOKEN, SV_DEV_BAD_TEMPERATURE, SV_DEV_BAD_KEEP_LEN, SV_DEV_BAD_OFFSETS, SV_DEV_NO_DRAFT_ROWS,
  SV_DEV_BAD_ALPHA, SV_DEV_BAD_DRAFT_LEN, SV_DEV_TIMEOUT) = (1 << b for b in range(8))
 SV_FLAG_Q_ZERO, SV_FLAG_Z_ZERO, SV_FLAG_INVALID = 1, 2, 4
-SV_KERNEL_VERIFY, SV_KERNEL_SCHEDULE, SV_NUM_KERNELS = range(3)
-KERNEL_NAMES = ("verify", "schedule")
+SV_KERNEL_ROW_STATS, SV_KERNEL_COMBINE, SV_KERNEL_SCHEDULE, SV_KERNEL_MASS, SV_KERNEL_PICK, SV_NUM_KERNELS = range(6)
+KERNEL_NAMES = ("row_stats", "combine", "schedule", "mass", "pick")
 
 _c = ctypes
 _vp, _i32, _i64, _u32, _u64, _f32, _sz = (_c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_uint64,
@@ -54,6 +54,7 @@ _SIGS = {
     "sv_schedule_depth_table": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _c.c_int,
                                            _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz,
                                            _vp]),
+    "sv_test_stall_next_verify": (None, [_c.c_int]),
     "sv_query_status": (_c.c_int, [_vp, _vp, _c.POINTER(_u32)]),
     "sv_status_string": (_c.c_char_p, [_c.c_int]),
     "sv_last_error_string": (_c.c_char_p, []),
@@ -286,6 +287,10 @@ def sv_schedule_depth_table(alpha, alpha_stride, draft_len, B, Dmax, cost_K, cos
                                          _p(out_keep_len), _p(out_row_offsets), _p(out_total_K),
                                          _p(out_utility_q48), _p(ws), _ws_bytes(ws),
                                          _stream(stream)))
+
+
+def sv_test_stall_next_verify(wait_limit_ms: int) -> None:
+    lib().sv_test_stall_next_verify(int(wait_limit_ms))
 
 
 def sv_query_status(ws, stream=None) -> tuple[int, int]:

@@ -68,29 +68,35 @@ cudaEvent_t take_event() {
   return e;
 }
 
+// Test hook (sv_test_stall_next_verify): wait limit in ms for the next verification call, 0 = none.
+std::atomic<int> g_stall_ms{0};
+
 // ---- shared verify entry ----------------------------------------------------------------------
-sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, void* ws, size_t ws_bytes, void* stream) {
+sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws, size_t ws_bytes,
+                        void* stream) {
   if (p.B == 0) return SV_OK;  // nothing to verify: no workspace needed, nothing enqueued
   int cl, nc;
   sv::vocab_tiling(p.V, dt, &cl, &nc);
-  // every (row, chunk) task and stream unit is counted in 32-bit integers
-  const int64_t tasks = static_cast<int64_t>(p.B) * (2 * static_cast<int64_t>(p.Kmax) + 1) * nc;
-  if (tasks > INT32_MAX) return fail(SV_ERR_INVALID_ARG, "B*(2K+1)*chunks = %lld exceeds 2^31 - 1", (long long)tasks);
   const sv::VerifyLayout L = sv::verify_layout(p.B, p.Kmax, nc);
   sv_status s = check_ws(ws, ws_bytes, L.total);
   if (s != SV_OK) return s;
   unsigned char* w = static_cast<unsigned char*>(ws);
   p.chunk_len = cl;
   p.nchunks = nc;
+  p.rows_per_req = 2 * p.Kmax + 1;
+  // Greedy fixed-K calls need no per-request plan: every request has the same rows.  Sampling
+  // calls take the per-request plan, which leaves out the draft rows of T == 0 requests.
+  if (p.keep_len == nullptr && p.t_off == nullptr && p.d_off == nullptr && p.temperature == nullptr)
+    p.uniform_rows = p.tokens == nullptr ? 2 * p.Kmax + 1 : p.Kmax + 1;
   p.status = reinterpret_cast<uint32_t*>(w + L.status);
-  p.done = reinterpret_cast<uint32_t*>(w + L.counters);
-  p.ready = p.done + SV_MAX_BATCH;
-  p.draw_done = p.ready + SV_MAX_BATCH;
+  const int stall_ms = g_stall_ms.exchange(0);
+  p.wait_limit_ns = stall_ms > 0 ? static_cast<uint64_t>(stall_ms) * 1000000ull : 2000000000ull;
+  p.stall_cta = stall_ms > 0 ? 1 : 0;
   p.req = reinterpret_cast<sv::ReqState*>(w + L.req);
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
   p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
-  const int e = sv::launch_verify(p, dt, stream);
+  const int e = sv::launch_verify(p, dt, sampled, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;
 }
@@ -171,6 +177,8 @@ extern "C" {
 
 int sv_abi_version(void) { return 2; }
 
+void sv_test_stall_next_verify(int wait_limit_ms) { g_stall_ms.store(wait_limit_ms > 0 ? wait_limit_ms : 0); }
+
 size_t sv_workspace_size(int op, int B, int Kmax, int V, sv_dtype dt) {
   if (op == SV_OP_SCHEDULE) return 256;
   if (op != SV_OP_VERIFY) return 0;
@@ -201,7 +209,7 @@ sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void*
   p.t_rows = p.d_rows = -1;
   p.out_tokens = out_tokens;
   p.out_accept_len = out_accept_len;
-  return verify_common(p, dt, ws, ws_bytes, stream);
+  return verify_common(p, dt, false, ws, ws_bytes, stream);
 }
 
 sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
@@ -232,7 +240,7 @@ sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void*
   p.out_q = out_q;
   p.out_flags = out_flags;
   p.t_rows = p.d_rows = -1;
-  return verify_common(p, dt, ws, ws_bytes, stream);
+  return verify_common(p, dt, true, ws, ws_bytes, stream);
 }
 
 sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets, int64_t t_rows,
@@ -280,7 +288,7 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
   p.out_p = out_p;
   p.out_q = out_q;
   p.out_flags = out_flags;
-  return verify_common(p, dt, ws, ws_bytes, stream);
+  return verify_common(p, dt, true, ws, ws_bytes, stream);
 }
 
 // Checks and launch shared by both scheduling entry points; p arrives with its cost

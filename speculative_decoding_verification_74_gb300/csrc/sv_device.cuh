@@ -158,32 +158,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of a phase (no suspend).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Add to a global counter with release semantics (every earlier write of this thread is
-// visible before the count is), without waiting for the result.
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait: gives up after ~2 s (or 2^24 polls), records SV_DEV_TIMEOUT and returns false.
+// Bounded wait: gives up after limit_ns (~2 s by default; or 2^24 polls), records
+// SV_DEV_TIMEOUT and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kWaitMaxPolls = 1u << 24;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   // a few quick polls, then back off with nanosleep so a waiting warp takes few issue slots;
   // the timer is read only once a wait runs long
   for (uint32_t it = 0; it < 4; ++it)
@@ -192,52 +177,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   for (uint32_t it = 4; it < kWaitMaxPolls; ++it) {
     __nanosleep(it < 64 ? 32 : 256);
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
-  }
-  atomicOr(status, SV_DEV_TIMEOUT);
-  return false;
-}
-// Bounded wait of a CTA that cooperates with the rest of the grid: as mbar_wait, but it also gives
-// up (without recording anything) as soon as this CTA's abort flag is set or another CTA has
-// recorded SV_DEV_TIMEOUT in the status word.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                                   const volatile int* abort_flag) {
-  for (uint32_t it = 0; it < 4; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 4; it < kWaitMaxPolls; ++it) {
-    __nanosleep(it < 64 ? 32 : 256);
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*abort_flag || (*reinterpret_cast<volatile uint32_t*>(status) & SV_DEV_TIMEOUT)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-    }
-  }
-  atomicOr(status, SV_DEV_TIMEOUT);
-  return false;
-}
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Bounded wait until a flag another CTA sets with st_release_u32 holds `expect` (acquire loads,
-// nanosleep backoff).  Gives up like mbar_wait_or_abort; on its own time limit it records
-// SV_DEV_TIMEOUT.
-__device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t expect, uint32_t* status,
-                                          const volatile int* abort_flag) {
-  if (ld_acquire_u32(flag) == expect) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1; it < kWaitMaxPolls; ++it) {
-    __nanosleep(it < 32 ? 64 : 256);
-    if (ld_acquire_u32(flag) == expect) return true;
-    if ((it & 15u) == 0) {
-      if (*abort_flag || (*reinterpret_cast<volatile uint32_t*>(status) & SV_DEV_TIMEOUT)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-    }
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
   }
   atomicOr(status, SV_DEV_TIMEOUT);
   return false;

@@ -7,20 +7,18 @@
 
 namespace sv {
 
-// ---- verification kernel geometry ---------------------------------------------------------
+// ---- row_stats kernel geometry ---------------------------------------------------------------
 constexpr int kStageBytes = 16384;     // one vocabulary chunk per pipeline stage
 constexpr int kStages = 4;             // bulk-copy ring depth
-constexpr int kConsumerWarps = 4;      // warps that reduce a chunk (8 vectors per thread)
+constexpr int kConsumerWarps = 4;      // warps that reduce a chunk (8 vectors per thread: the
+                                       // per-chunk bookkeeping is spread over 64 logits)
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kVerifyThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kStatsThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;  // 16-byte vectors per thread
 static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split");
-// Each vocabulary chunk's draw weights are summed in kDrawRanges contiguous ranges; the pick
-// finds the crossing range among them and scans only that range.
-constexpr int kDrawRanges = 8;
-static_assert(kDrawRanges == kVecPerThread, "a full chunk's range r is every thread's vector r");
 
-// Per-(row, chunk) statistics of the stream.
+
+// Per-(row, chunk) statistics written by row_stats.
 struct alignas(16) ChunkRecord {
   float m;     // max logit in the chunk
   float s;     // sum of 2^(x k - rint(m k)) over the chunk, k = log2(e) / T (0 for greedy rows)
@@ -28,8 +26,8 @@ struct alignas(16) ChunkRecord {
   float xval;  // logit at the row's drafted token, when that token lies in the chunk
 };
 
-// What the draw at the accepted length needs: written by the CTA that runs a request's accept
-// chain, read by the draw units and the pick.
+// What the draw at the accepted length needs (written by the combine kernel, read by the mass and
+// pick kernels).
 enum : int32_t { kModeNone = 0, kModeBonus = 1, kModeResidual = 2 };
 struct alignas(16) ReqState {
   int32_t mode;
@@ -61,8 +59,7 @@ struct VerifyParams {
   uint32_t round;
   int32_t B, Kmax, V;
   int32_t chunk_len, nchunks;  // vocabulary tiling
-  int32_t unit_tasks;          // (row, chunk) tasks per stream unit
-  int32_t delay_units;         // stream units between a request's last stream unit and its draw
+  int32_t rows_per_req;        // 2 * Kmax + 1 record rows per request
   // outputs
   int32_t* out_tokens;      // [B, Kmax+1]
   int32_t* out_accept_len;  // [B]
@@ -70,14 +67,15 @@ struct VerifyParams {
   float* out_q;
   uint8_t* out_flags;       // [B] nullable
   // workspace
-  uint32_t* status;         // [0] status word, [1] unit counter, [2] finished-CTA counter, [3] call tag
-  uint32_t* done;           // [B] stream tasks finished
-  uint32_t* ready;          // [B] draw state published (holds the call tag + 1)
-  uint32_t* draw_done;      // [B] draw units finished
+  uint32_t* status;
   ReqState* req;            // [B] draw state per request
-  ChunkRecord* rec;         // [B * (2 Kmax + 1) * nchunks]
-  float* mass;              // [B * nchunks * kDrawRanges] residual mass per draw range
-  float* mass_p;            // [B * nchunks * kDrawRanges] target-row weight per draw range
+  ChunkRecord* rec;         // [B * rows_per_req * nchunks]
+  float* mass;              // [B * nchunks * 8] residual mass per draw range (8 per chunk)
+  float* mass_p;            // [B * nchunks * 8] target-row weight per draw range (bonus / fallback)
+  uint64_t wait_limit_ns;   // bound of every wait in the stream kernel
+  int32_t stall_cta;        // test hook: > 0 makes CTA stall_cta - 1 of the stream issue no copy
+  int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
+  int32_t fuse_draw;        // 1: the combine kernel's CTAs also sum the draw weights per chunk
 };
 
 // Largest B * Dmax ranked by merging the per-request runs (two key buffers in shared memory);
@@ -109,17 +107,15 @@ struct ScheduleParams {
   uint32_t* status;
 };
 
-// Workspace layout for SV_OP_VERIFY.  The status region and the per-request counters come
-// first, at the same place for every batch size; they must be zero before the first call, and
-// a call that completes leaves the counters zero.
+// Workspace layout for SV_OP_VERIFY.
 struct VerifyLayout {
-  size_t status, counters, req, mass, mass_p, rec, total;
+  size_t status, req, rec, mass, mass_p, total;
 };
 VerifyLayout verify_layout(int B, int Kmax, int nchunks);
 void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);
 
 // Launchers (return cudaError_t as int to keep CUDA headers out of this file).
-int launch_verify(const VerifyParams& p, sv_dtype dt, void* stream);
+int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream);
 int launch_schedule(const ScheduleParams& p, void* stream);
 
 // Host-side argument checks of sv_verify_sample (sv_api.cu); touch no GPU.

@@ -63,9 +63,8 @@ extern "C" sv_status sv_verify_sample_noalloc(const void* target, int64_t t_row_
   if (e != cudaSuccess) {
     return sv::set_error(SV_ERR_CUDA, "scratch address: %s", cudaGetErrorString(e));
   }
-  // The array keeps the previous call's contents: the status word and the per-request
-  // completion counters, which lie before the draw state, must start at zero (everything else
-  // is written before it is read).
+  // The array keeps the previous call's contents: the status word must start at zero
+  // (everything else is written before it is read).
   int cl, nc;
   sv::vocab_tiling(V, dt, &cl, &nc);
   const sv::VerifyLayout L = sv::verify_layout(B, K, nc);
