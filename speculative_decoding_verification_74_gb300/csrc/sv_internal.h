@@ -9,7 +9,15 @@ namespace sv {
 
 // ---- row_stats kernel geometry ---------------------------------------------------------------
 constexpr int kStageBytes = 16384;     // one vocabulary chunk per pipeline stage
-constexpr int kStages = 4;             // bulk-copy ring depth
+// Bulk-copy ring depth and resident CTAs per SM of the streaming kernel, per logit type: fp32
+// chunks (4096 logits) leave the consumers idle between copies, so 3 CTAs of 4 stages keep HBM
+// busy; bf16 chunks (8192 logits) are bound by instruction issue, so 4 CTAs of 3 stages (the same
+// bytes in flight per SM) add warps.
+template <int DT>
+struct StreamShape {
+  static constexpr int kStages = DT == SV_BF16 ? 3 : 4;
+  static constexpr int kCtasPerSm = DT == SV_BF16 ? 4 : 3;
+};
 constexpr int kConsumerWarps = 4;      // warps that reduce a chunk (8 vectors per thread: the
                                        // per-chunk bookkeeping is spread over 64 logits)
 constexpr int kConsumerThreads = kConsumerWarps * 32;

@@ -209,9 +209,12 @@ struct StatsRed {
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) row_stats_kernel(const VerifyParams p) {
+  constexpr int kStages = StreamShape<DT>::kStages;
   constexpr int kElt = DT == SV_BF16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;  // elements per 16-byte vector
+  // -inf in every element of a padding vector
+  constexpr uint32_t kPadWord = DT == SV_BF16 ? 0xFF80FF80u : 0xFF800000u;
   extern __shared__ __align__(128) unsigned char smem[];
   const int B = p.B, Kmax = p.Kmax, NC = p.nchunks, R = p.rows_per_req;
   unsigned char* stages = smem;
@@ -378,10 +381,15 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
     named_bar(2, kConsumerThreads);
     const unsigned char* sb = stages + stage * kStageBytes;
     uint4 raw[kVecPerThread];
+    if (DT == SV_BF16 && nvec == kVecPerThread * kConsumerThreads) {  // a full bf16 chunk: no predicates
 #pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j) {
-      const int v = tid + j * kConsumerThreads;
-      raw[j] = v < nvec ? lds128(sb + v * 16) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+      for (int j = 0; j < kVecPerThread; ++j) raw[j] = lds128(sb + (tid + j * kConsumerThreads) * 16);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j) {
+        const int v = tid + j * kConsumerThreads;
+        raw[j] = v < nvec ? lds128(sb + v * 16) : make_uint4(kPadWord, kPadWord, kPadWord, kPadWord);
+      }
     }
     float xval = NAN;
     if (tid == 0 && tok >= v0 && tok < te) {
@@ -471,23 +479,23 @@ __global__ void __launch_bounds__(kStatsThreads, 3) row_stats_kernel(const Verif
       }
       if (m != -INFINITY) {
         // terms 2^(x k - c): one fused multiply-add per logit, done on pairs of logits in
-        // packed f32x2 registers; even and odd positions keep separate sums
+        // packed f32x2 registers; even and odd positions keep separate sums.  Padding vectors
+        // hold -inf, whose term is 2^-inf = 0: bf16 needs no predicate per vector (fp32 keeps
+        // one, which measured faster there).
         const f32x2 k2 = f2_pack(kscale, kscale), nc2 = f2_pack(-cofs, -cofs);
         f32x2 acc2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};  // two independent chains
 #pragma unroll
         for (int j = 0; j < kVecPerThread; ++j) {
-          if (tid + j * kConsumerThreads < nvec) {
-            if constexpr (DT == SV_BF16) {
-              const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+          if constexpr (DT == SV_BF16) {
+            const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                acc2[e & 1] = f2_add(acc2[e & 1], f2_exp2_offset(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), k2, nc2));
-            } else {
-              acc2[0] = f2_add(acc2[0], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].x),
-                                                               __uint_as_float(raw[j].y)), k2, nc2));
-              acc2[1] = f2_add(acc2[1], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].z),
-                                                               __uint_as_float(raw[j].w)), k2, nc2));
-            }
+            for (int e = 0; e < 4; ++e)
+              acc2[e & 1] = f2_add(acc2[e & 1], f2_exp2_offset(f2_pack(bf16_lo(w[e]), bf16_hi(w[e])), k2, nc2));
+          } else if (tid + j * kConsumerThreads < nvec) {
+            acc2[0] = f2_add(acc2[0], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].x),
+                                                             __uint_as_float(raw[j].y)), k2, nc2));
+            acc2[1] = f2_add(acc2[1], f2_exp2_offset(f2_pack(__uint_as_float(raw[j].z),
+                                                             __uint_as_float(raw[j].w)), k2, nc2));
           }
         }
         float a0, a1, a2, a3;
@@ -1163,7 +1171,8 @@ cudaError_t device_setup(int* num_sms) {
   if (!ds.ready[di]) {
     if (ds.num_sms == 0 && (e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
-    const size_t max_dyn = static_cast<size_t>(kStages) * kStageBytes + (SV_MAX_BATCH + 4) * 4 + SV_MAX_BATCH * 2;
+    const size_t max_dyn =
+        static_cast<size_t>(StreamShape<DT>::kStages) * kStageBytes + (SV_MAX_BATCH + 4) * 4 + SV_MAX_BATCH * 2;
     if ((e = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(max_dyn))) != cudaSuccess)
       return e;
@@ -1203,7 +1212,7 @@ template <int DT>
 cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
   const size_t table =
       p.uniform_rows > 0 ? 0 : static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
-  const size_t dyn = static_cast<size_t>(kStages) * kStageBytes + table;
+  const size_t dyn = static_cast<size_t>(StreamShape<DT>::kStages) * kStageBytes + table;
   cudaError_t e;
   int num_sms = 0;
   if ((e = device_setup<DT>(&num_sms)) != cudaSuccess) return e;
