@@ -66,7 +66,7 @@ typedef enum {
 typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
 
 /* operation ids for sv_workspace_size */
-enum { SV_OP_VERIFY = 0, SV_OP_SCHEDULE = 1 };
+enum { SV_OP_VERIFY = 0, SV_OP_SCHEDULE = 1, SV_OP_TREE = 2 };
 
 /* objective of sv_schedule_depth */
 enum {
@@ -83,7 +83,8 @@ enum {
   SV_DEV_NO_DRAFT_ROWS = 1u << 4,   /* T > 0 (or greedy without tokens) but draft NULL */
   SV_DEV_BAD_ALPHA = 1u << 5,       /* confidence outside [0, 1] or NaN              */
   SV_DEV_BAD_DRAFT_LEN = 1u << 6,   /* draft_len outside [0, Dmax]                   */
-  SV_DEV_TIMEOUT = 1u << 7          /* a bounded wait inside a kernel ran out        */
+  SV_DEV_TIMEOUT = 1u << 7,         /* a bounded wait inside a kernel ran out        */
+  SV_DEV_BAD_PARENT = 1u << 8       /* tree node whose parent is not an earlier node */
 };
 
 /* per-request bits of out_flags */
@@ -188,6 +189,49 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
                            int B, int Kmax, int V, int32_t* out_tokens, int32_t* out_accept_len,
                            float* out_p, float* out_q, uint8_t* out_flags, void* ws,
                            size_t ws_bytes, void* stream);
+
+/*
+ * sv_verify_tree -- multi-candidate (token tree) verification by multi-step
+ * speculative sampling (Miao et al., "SpecInfer", ASPLOS 2024, section 4.2);
+ * a chain-shaped tree is exactly sv_verify_ragged ([explainer] "DFly": the
+ * draft block is one causal chain; "D-cut": verification stays lossless).
+ *
+ * Request i has N_i = node_offsets[i+1] - node_offsets[i] nodes, 1 <= N_i <=
+ * Nmax, in an order where each parent precedes its children; node 0 is the
+ * root (the verified context).  With o = node_offsets[i] (device int32 [B+1]):
+ *   parent[o + c]  (1 <= c < N_i): the parent node of node c, 0 <= parent < c
+ *   tokens[o + c]  (1 <= c < N_i): node c's drafted token, in [0, V)
+ *   target + (o + c) * t_row_stride: target logits of the token after node c's path
+ *   draft  + (o + c) * d_row_stride: the draft logits node c's children were drafted from
+ * (entries c = 0 of parent / tokens and the draft rows of leaves are not read).
+ * n_rows is the number of rows both arrays hold; every request's rows must lie
+ * below it (else SV_DEV_BAD_OFFSETS).
+ *
+ * Per request with T = temperature[i], walking from the root: at a node with
+ * children x_1..x_m (in node order), p = softmax(target/T), q = softmax(draft/T):
+ *   p' = p; for j = 1..m: accept x_j iff u_j * q(x_j) < p'(x_j), u_j =
+ *   Philox(purpose 0, position = node index of x_j minus 1); on a rejection
+ *   p' = norm(max(0, p' - q)).  An accepted child is emitted and the walk goes
+ *   on from it; if all are rejected, y ~ p' is drawn by inverse CDF in vocabulary
+ *   order (u' = Philox(purpose 1, position = the node's index)) and the walk
+ *   stops.  At a node without children y ~ p (the bonus draw).  T == 0: the
+ *   first child equal to the target argmax (lowest index on ties) is accepted;
+ *   otherwise the argmax is emitted and the walk stops.  Draft rows are read only
+ *   for T > 0 (draft may be NULL when every T is 0).
+ * Outputs (device): out_path [B, Nmax] int32: the accepted nodes (root
+ * excluded) then -1; out_tokens [B, Nmax] int32: their tokens, then y, then -1;
+ * out_accept_len [B]: accepted nodes; out_flags [B] (nullable): SV_FLAG_* bits.
+ * Workspace: sv_workspace_size(SV_OP_TREE, B, Nmax, V, dt).  Invalid requests
+ * get -1 outputs, SV_FLAG_INVALID and a SV_DEV_* bit (bad parents:
+ * SV_DEV_BAD_PARENT, bad tokens: SV_DEV_BAD_TOKEN, N_i outside [1, Nmax]:
+ * SV_DEV_BAD_KEEP_LEN).
+ */
+sv_status sv_verify_tree(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                         const int32_t* node_offsets, int64_t n_rows, const int32_t* parent,
+                         const int32_t* tokens, const float* temperature, uint64_t seed, uint32_t round,
+                         const int32_t* request_ids, sv_dtype dt, int B, int Nmax, int V,
+                         int32_t* out_path, int32_t* out_tokens, int32_t* out_accept_len,
+                         uint8_t* out_flags, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * sv_schedule_depth -- D-cut batch-shared verification-depth allocation
@@ -309,7 +353,8 @@ enum {
   SV_KERNEL_SCHEDULE = 2,  /* D-cut depth allocation                                      */
   SV_KERNEL_MASS = 3,      /* per-chunk draw weights for long requests                    */
   SV_KERNEL_PICK = 4,      /* inverse-CDF draw                                            */
-  SV_NUM_KERNELS = 5
+  SV_KERNEL_TREE_WALK = 5, /* tree verification: the walk from the root                   */
+  SV_NUM_KERNELS = 6
 };
 void sv_profile_enable(int on);
 sv_status sv_profile_collect(double* total_ms, int64_t* launches);

@@ -23,4 +23,4 @@ from .verify import (softmax_T, verify_request, verify_batch, request_uniforms, 
 from .schedule import (prefix_confidences, k_rho, candidate_budgets, dcut_schedule, table_cost,
                        check_cost_table)
 from .metrics import mean_accepted_length, mean_acceptance, expected_accept_len
-from .tree import verify_tree, children_of
+from .tree import verify_tree, verify_tree_batch, children_of

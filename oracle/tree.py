@@ -39,7 +39,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .verify import softmax_T, FLAG_Q_ZERO, FLAG_Z_ZERO, NEAR_ACCEPT, NEAR_PICK, NEAR_TOL
+from .verify import (softmax_T, decode_rows, request_uniforms, FLAG_Q_ZERO, FLAG_Z_ZERO, NEAR_ACCEPT, NEAR_PICK,
+                     NEAR_TOL)
 
 
 def children_of(parent) -> list[list[int]]:
@@ -116,3 +117,22 @@ def verify_tree(parent, token, t, d, T, u_acc, u_res) -> dict:
             return out(y)
         path.append(accepted)
         node = accepted
+
+
+def verify_tree_batch(target, draft, node_offsets, parent, tokens, temperature, seed, rnd, request_ids, dtype):
+    """Verify a packed batch of trees (the library's layout: node c of request i is row
+    node_offsets[i] + c of target and draft, and entry node_offsets[i] + c of parent and tokens),
+    request by request.  Uniforms: the accept test of child c uses position c - 1, the draw at node
+    n position n, as in the chain (request_uniforms with n = N - 1).  Returns one verify_tree
+    result per request."""
+    out = []
+    for i in range(len(node_offsets) - 1):
+        a, b = int(node_offsets[i]), int(node_offsets[i + 1])
+        N = b - a
+        T = float(np.float32(temperature[i]))
+        t = list(decode_rows(target[a:b], dtype))
+        d = list(decode_rows(draft[a:b], dtype)) if T > 0.0 else [None] * N
+        rid = int(request_ids[i]) if request_ids is not None else i
+        u_acc, u_res = request_uniforms(seed, rid, rnd, N - 1)
+        out.append(verify_tree(np.asarray(parent[a:b]), np.asarray(tokens[a:b]), t, d, T, u_acc, u_res))
+    return out

@@ -25,13 +25,14 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "sv.h")
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT = range(6)
 SV_BF16, SV_F32 = 0, 1
-SV_OP_VERIFY, SV_OP_SCHEDULE = 0, 1
+SV_OP_VERIFY, SV_OP_SCHEDULE, SV_OP_TREE = 0, 1, 2
 SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
 (SV_DEV_BAD_TOKEN, SV_DEV_BAD_TEMPERATURE, SV_DEV_BAD_KEEP_LEN, SV_DEV_BAD_OFFSETS, SV_DEV_NO_DRAFT_ROWS,
- SV_DEV_BAD_ALPHA, SV_DEV_BAD_DRAFT_LEN, SV_DEV_TIMEOUT) = (1 << b for b in range(8))
+ SV_DEV_BAD_ALPHA, SV_DEV_BAD_DRAFT_LEN, SV_DEV_TIMEOUT, SV_DEV_BAD_PARENT) = (1 << b for b in range(9))
 SV_FLAG_Q_ZERO, SV_FLAG_Z_ZERO, SV_FLAG_INVALID = 1, 2, 4
-SV_KERNEL_ROW_STATS, SV_KERNEL_COMBINE, SV_KERNEL_SCHEDULE, SV_KERNEL_MASS, SV_KERNEL_PICK, SV_NUM_KERNELS = range(6)
-KERNEL_NAMES = ("row_stats", "combine", "schedule", "mass", "pick")
+(SV_KERNEL_ROW_STATS, SV_KERNEL_COMBINE, SV_KERNEL_SCHEDULE, SV_KERNEL_MASS, SV_KERNEL_PICK, SV_KERNEL_TREE_WALK,
+ SV_NUM_KERNELS) = range(7)
+KERNEL_NAMES = ("row_stats", "combine", "schedule", "mass", "pick", "tree_walk")
 
 _c = ctypes
 _vp, _i32, _i64, _u32, _u64, _f32, _sz = (_c.c_void_p, _c.c_int32, _c.c_int64, _c.c_uint32, _c.c_uint64,
@@ -54,6 +55,8 @@ _SIGS = {
     "sv_schedule_depth_table": (_c.c_int, [_vp, _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _c.c_int,
                                            _c.c_int, _vp, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz,
                                            _vp]),
+    "sv_verify_tree": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _u64, _u32, _vp, _c.c_int,
+                                  _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sv_test_stall_next_verify": (None, [_c.c_int]),
     "sv_query_status": (_c.c_int, [_vp, _vp, _c.POINTER(_u32)]),
     "sv_status_string": (_c.c_char_p, [_c.c_int]),
@@ -289,6 +292,29 @@ def sv_schedule_depth_table(alpha, alpha_stride, draft_len, B, Dmax, cost_K, cos
                                          _stream(stream)))
 
 
+def sv_verify_tree(target, t_row_stride, draft, d_row_stride, node_offsets, n_rows, parent, tokens, temperature,
+                   seed, round_, request_ids, dt, B, Nmax, V, out_path, out_tokens, out_accept_len, out_flags, ws,
+                   stream=None) -> None:
+    if B > 0:
+        # the packed arrays hold n_rows rows; the kernels bound every request's rows by it
+        _need_rows(target, "target", dt, n_rows, t_row_stride, V)
+        if draft is not None:
+            _need_rows(draft, "draft", dt, n_rows, d_row_stride, V)
+        _need(node_offsets, "node_offsets", torch.int32, B + 1)
+        _need(parent, "parent", torch.int32, n_rows)
+        _need(tokens, "tokens", torch.int32, n_rows)
+        _need(temperature, "temperature", torch.float32, B)
+        _need(request_ids, "request_ids", torch.int32, B)
+        _need(out_path, "out_path", torch.int32, B * Nmax)
+        _need(out_tokens, "out_tokens", torch.int32, B * Nmax)
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
+        _need(out_flags, "out_flags", torch.uint8, B)
+    _check(lib().sv_verify_tree(_p(target), t_row_stride, _p(draft), d_row_stride, _p(node_offsets), n_rows,
+                                _p(parent), _p(tokens), _p(temperature), seed & (2 ** 64 - 1), round_,
+                                _p(request_ids), dt, B, Nmax, V, _p(out_path), _p(out_tokens), _p(out_accept_len),
+                                _p(out_flags), _p(ws), _ws_bytes(ws), _stream(stream)))
+
+
 def sv_test_stall_next_verify(wait_limit_ms: int) -> None:
     lib().sv_test_stall_next_verify(int(wait_limit_ms))
 
@@ -378,6 +404,28 @@ def verify_sample(target, draft, draft_tokens, temperature, K, *, seed=0, round_
     sv_verify_sample(target, _rows(target)[1], draft, ds, draft_tokens, temperature, seed, round_, request_ids,
                      dt, B, K, V, out_tok, out_len, out_p, out_q, out_f, ws, stream)
     return out_tok, out_len, out_p, out_q, out_f
+
+
+def verify_tree(target, draft, node_offsets, parent, tokens, temperature, Nmax, *, seed=0, round_=0,
+                request_ids=None, ws=None, stream=None, out=None):
+    """Token-tree verification.  target / draft [rows, V]: node c of request i is row
+    node_offsets[i] + c; parent / tokens [rows] int32 per node; temperature [B].  Returns
+    (path [B, Nmax], tokens [B, Nmax], accept_len [B], flags [B])."""
+    V = target.shape[-1]
+    B = node_offsets.numel() - 1
+    dt = _dt(target)
+    dev = target.device
+    if out is None:
+        out = (torch.empty((B, Nmax), dtype=torch.int32, device=dev),
+               torch.empty((B, Nmax), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.uint8, device=dev))
+    if ws is None:
+        ws = workspace(SV_OP_TREE, B, Nmax, V, dt, dev)
+    ds = _rows(draft)[1] if draft is not None else V
+    sv_verify_tree(target, _rows(target)[1], draft, ds, node_offsets, num_rows(target), parent, tokens, temperature,
+                   seed, round_, request_ids, dt, B, Nmax, V, *out, ws, stream)
+    return out
 
 
 def verify_ragged(target, t_row_offsets, draft, d_row_offsets, draft_tokens, keep_len, temperature, Kmax, *,

@@ -96,7 +96,7 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
   p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
-  const int e = sv::launch_verify(p, dt, sampled, stream);
+  const int e = p.tree ? sv::launch_tree(p, dt, stream) : sv::launch_verify(p, dt, sampled, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;
 }
@@ -181,7 +181,12 @@ void sv_test_stall_next_verify(int wait_limit_ms) { g_stall_ms.store(wait_limit_
 
 size_t sv_workspace_size(int op, int B, int Kmax, int V, sv_dtype dt) {
   if (op == SV_OP_SCHEDULE) return 256;
-  if (op != SV_OP_VERIFY) return 0;
+  if (op == SV_OP_TREE) {  // Kmax is Nmax here: a tree of N nodes has the rows of a chain of N - 1
+    if (Kmax < 1) return 0;
+    --Kmax;
+  } else if (op != SV_OP_VERIFY) {
+    return 0;
+  }
   if (B < 0 || B > SV_MAX_BATCH || Kmax < 0 || Kmax > SV_MAX_DRAFT || V < 1 || V > (1 << 30)) return 0;
   if (dt != SV_BF16 && dt != SV_F32) return 0;
   int cl, nc;
@@ -287,6 +292,47 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
   p.out_accept_len = out_accept_len;
   p.out_p = out_p;
   p.out_q = out_q;
+  p.out_flags = out_flags;
+  return verify_common(p, dt, true, ws, ws_bytes, stream);
+}
+
+sv_status sv_verify_tree(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                         const int32_t* node_offsets, int64_t n_rows, const int32_t* parent, const int32_t* tokens,
+                         const float* temperature, uint64_t seed, uint32_t round, const int32_t* request_ids,
+                         sv_dtype dt, int B, int Nmax, int V, int32_t* out_path, int32_t* out_tokens,
+                         int32_t* out_accept_len, uint8_t* out_flags, void* ws, size_t ws_bytes, void* stream) {
+  if (Nmax < 1 || Nmax > SV_MAX_DRAFT + 1)
+    return fail(SV_ERR_INVALID_ARG, "Nmax=%d outside [1, %d]", Nmax, SV_MAX_DRAFT + 1);
+  sv_status s = check_common(target, t_row_stride, draft, d_row_stride, dt, B, Nmax - 1, V, out_tokens,
+                             out_accept_len);
+  if (s != SV_OK) return s;
+  if (B > 0) {
+    if (node_offsets == nullptr || parent == nullptr || tokens == nullptr || out_path == nullptr)
+      return fail(SV_ERR_INVALID_ARG, "node_offsets, parent, tokens and out_path are required");
+    if (n_rows < 0) return fail(SV_ERR_INVALID_ARG, "n_rows must be >= 0");
+  }
+  sv::VerifyParams p = {};
+  p.tree = 1;
+  p.target = target;
+  p.t_row_stride = t_row_stride;
+  p.t_off = node_offsets;
+  p.t_rows = n_rows;
+  p.draft = draft;
+  p.d_row_stride = d_row_stride;
+  p.d_off = node_offsets;
+  p.d_rows = draft != nullptr ? n_rows : 0;
+  p.tree_parent = parent;
+  p.tree_tokens = tokens;
+  p.temperature = temperature;
+  p.request_ids = request_ids;
+  p.seed = seed;
+  p.round = round;
+  p.B = B;
+  p.Kmax = Nmax - 1;
+  p.V = V;
+  p.out_tokens = out_tokens;
+  p.out_path = out_path;
+  p.out_accept_len = out_accept_len;
   p.out_flags = out_flags;
   return verify_common(p, dt, true, ws, ws_bytes, stream);
 }

@@ -26,6 +26,10 @@ constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;  // 16-byte v
 static_assert(kVecPerThread * 16 * kConsumerThreads == kStageBytes, "stage split");
 
 
+// Each vocabulary chunk's draw weights are summed in kDrawRanges contiguous ranges (one per
+// warp); a pick finds the crossing range and scans only that range.
+constexpr int kDrawRanges = 8;
+
 // Per-(row, chunk) statistics written by row_stats.
 struct alignas(16) ChunkRecord {
   float m;     // max logit in the chunk
@@ -80,6 +84,11 @@ struct VerifyParams {
   ChunkRecord* rec;         // [B * rows_per_req * nchunks]
   float* mass;              // [B * nchunks * 8] residual mass per draw range (8 per chunk)
   float* mass_p;            // [B * nchunks * 8] target-row weight per draw range (bonus / fallback)
+  // tree verification: the stream runs on every node row (n_i = N_i - 1 from t_off, no tokens)
+  int32_t tree;
+  const int32_t* tree_parent;  // [sum N_i] parent node per node
+  const int32_t* tree_tokens;  // [sum N_i] drafted token per node
+  int32_t* out_path;           // [B, Kmax + 1] accepted nodes
   uint64_t wait_limit_ns;   // bound of every wait in the stream kernel
   int32_t stall_cta;        // test hook: > 0 makes CTA stall_cta - 1 of the stream issue no copy
   int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
@@ -124,6 +133,10 @@ void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);
 
 // Launchers (return cudaError_t as int to keep CUDA headers out of this file).
 int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream);
+// The streaming kernel alone (its records feed the tree walk).
+int launch_stats(const VerifyParams& p, sv_dtype dt, void* stream);
+// Tree verification: the streaming kernel, then the walk kernel behind it.
+int launch_tree(const VerifyParams& p, sv_dtype dt, void* stream);
 int launch_schedule(const ScheduleParams& p, void* stream);
 
 // Host-side argument checks of sv_verify_sample (sv_api.cu); touch no GPU.

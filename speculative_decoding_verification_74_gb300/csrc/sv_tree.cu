@@ -1,0 +1,529 @@
+// Tree (multi-candidate) verification of libsv: multi-step speculative sampling (Miao et al.,
+// "SpecInfer: Accelerating Large Language Model Serving with Tree-based Speculative Inference and
+// Verification", ASPLOS 2024, section 4.2) over a token tree per request.
+//
+// The streaming kernel first reduces every node row of the call (target rows of all nodes, draft
+// rows of the sampled requests' nodes) into chunk records, as it does for a chain.  The walk
+// kernel then runs one CTA per request from the root:
+//   * a node's row statistics come from its chunk records (max, sum of 2^(x k - c), argmax);
+//   * the accept test of a child needs p and q at the child's token only: two logits;
+//   * after j rejections at a node, the renormalised residual p' = norm(max(0, p' - q)) is
+//     max(0, p - a_j q) / N_j with a_0 = 0, N_0 = 1, a_{j+1} = a_j + N_j and
+//     N_{j+1} = sum_v max(0, p_v - a_{j+1} q_v) (induction on j: max(0, max(0, p - a q) / N - q)
+//     = max(0, p - (a + N) q) / N).  So a rejection costs one pass over the node's target and draft
+//     rows, which sums the weights in 8 ranges per vocabulary chunk; the pass after the last
+//     rejection also serves the draw: the crossing range among the range sums, then a scan of it.
+// The passes stream the two rows through a 4-stage ring of 1-D bulk copies (cp.async.bulk).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr float kLog2eF = 1.44269504088896340736f;
+constexpr int kWalkThreads = 256;
+constexpr int kWalkWarps = kWalkThreads / 32;
+constexpr int kWalkStages = 4;  // ring of (target chunk, draft chunk) pairs
+static_assert(kWalkWarps == kDrawRanges, "one draw range of a chunk per warp");
+
+__device__ __forceinline__ float kscale_of(float T) { return __fdiv_rn(kLog2eF, T); }
+
+template <int DT>
+__device__ __forceinline__ const char* node_row(const void* base, int64_t row, int64_t stride) {
+  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
+  return reinterpret_cast<const char*>(base) + row * stride * kElt;
+}
+
+// A range [c0, c0 + len) of a row as a head of plain loads, a 16-byte aligned interior of nvec
+// vectors (the part a bulk copy can move) and a tail.
+struct Split {
+  int head, nvec, tail;
+};
+template <int kElt>
+__device__ __forceinline__ Split split_range(const char* row, int c0, int len) {
+  const uintptr_t s = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(c0) * kElt;
+  const uintptr_t e = s + static_cast<uintptr_t>(len) * kElt;
+  const uintptr_t a = (s + 15u) & ~uintptr_t(15), z = e & ~uintptr_t(15);
+  if (z <= a) return Split{len, 0, 0};
+  return Split{static_cast<int>((a - s) / kElt), static_cast<int>((z - a) / 16), static_cast<int>((e - z) / kElt)};
+}
+
+// Element e (chunk-relative) of a staged chunk: from the stage inside the copied interior, else
+// from the row.
+template <int DT>
+__device__ __forceinline__ float staged(const unsigned char* sb, const char* row, int c0, int e, const Split& sp) {
+  constexpr int kVec = DT == SV_BF16 ? 8 : 4;
+  if (e >= sp.head && e < sp.head + sp.nvec * kVec) {
+    if constexpr (DT == SV_BF16)
+      return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[e - sp.head]) << 16);
+    else
+      return reinterpret_cast<const float*>(sb)[e - sp.head];
+  }
+  return load_logit<DT>(row, c0 + e);
+}
+
+__device__ __forceinline__ void range_of(int len, int r, int* lo, int* hi) {
+  const int seg = (len + kDrawRanges - 1) / kDrawRanges;
+  *lo = min(len, r * seg);
+  *hi = min(len, *lo + seg);
+}
+
+__device__ __forceinline__ ChunkRecord ld_rec(const ChunkRecord* r) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(r));
+  return ChunkRecord{v.x, v.y, __float_as_int(v.z), v.w};
+}
+
+__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bb = __fsub_rn(s, hi);
+  lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb)));
+  hi = s;
+}
+
+// Row statistics from a row's chunk records, by one warp: max and (sampled) the sum of
+// 2^(x k - c(max)), or (greedy) the first argmax.
+__device__ void merge_row(const ChunkRecord* rr, int NC, bool sampled, float kscale, float* m_out, float* s_out,
+                          int* g_out) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  int g = -1;
+  for (int c = lane; c < NC; c += 32) {
+    const ChunkRecord rc = ld_rec(rr + c);
+    if (sampled) m = fmaxf(m, rc.m);
+    else merge_argmax(m, g, rc.m, rc.g);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    if (sampled) {
+      m = fmaxf(m, m2);
+    } else {
+      const int g2 = __shfl_xor_sync(0xFFFFFFFFu, g, o);
+      merge_argmax(m, g, m2, g2);
+    }
+  }
+  float S = 0.0f;
+  if (sampled && m != -INFINITY) {
+    const float C = exp_offset(m, kscale);
+    float hi = 0.0f, lo = 0.0f;
+    for (int c = lane; c < NC; c += 32) {
+      const ChunkRecord rc = ld_rec(rr + c);
+      if (rc.m != -INFINITY) two_sum_add(hi, lo, rc.s * pow2_nonpos(exp_offset(rc.m, kscale) - C));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o), l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+      two_sum_add(hi, lo, h2);
+      lo += l2;
+    }
+    S = hi + lo;
+  }
+  *m_out = m;
+  *s_out = S;
+  *g_out = g;
+}
+
+// The draw weights of a node: bonus  w_v = 2^(t_v k - ct)  (p up to a factor),
+//                             residual w_v = max(0, 2^(t_v k - ct) / St - a 2^(d_v k - cd) / Sd).
+struct Weights {
+  bool residual;
+  float kscale, ct, cd, inv_st, qs;  // qs = a / Sd
+};
+__device__ __forceinline__ float weight(float tx, float dx, const Weights& w) {
+  const float pv = ex2_approx(__fmaf_rn(tx, w.kscale, -w.ct));
+  if (!w.residual) return pv;
+  return fmaxf(0.0f, __fmaf_rn(pv, w.inv_st, -ex2_approx(__fmaf_rn(dx, w.kscale, -w.cd)) * w.qs));
+}
+
+struct WalkSmem {
+  float mt, st, md, sd;  // row statistics of the current node
+  int gt;
+  int accept;            // the current child's test
+  float Z;               // the last pass's total weight
+  int y;                 // the drawn / emitted token
+  uint32_t flags, bad;
+  int stop;              // the walk is over (or was aborted)
+  int aborted;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyParams p) {
+  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;  // [kWalkStages][2][kStageBytes]
+  const int Nmax = p.Kmax + 1;
+  int* par = reinterpret_cast<int*>(smem + static_cast<size_t>(kWalkStages) * 2 * kStageBytes);  // [Nmax]
+  int* tokn = par + Nmax;   // [Nmax]
+  int* first = tokn + Nmax; // [Nmax] first child (-1 none)
+  int* next = first + Nmax; // [Nmax] next sibling (-1 none)
+  int* path = next + Nmax;  // [Nmax]
+  __shared__ __align__(8) uint64_t full_bar[kWalkStages];
+  __shared__ WalkSmem ws;
+  pdl_wait();  // the streaming kernel's records are complete
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x;
+  const int NC = p.nchunks, R = 2 * p.Kmax + 1;
+  int32_t* out_path = p.out_path + static_cast<int64_t>(i) * Nmax;
+  int32_t* out_tok = p.out_tokens + static_cast<int64_t>(i) * Nmax;
+
+  // ---- the request: validity, nodes, parents, tokens, child lists ----
+  const int o = __ldg(p.t_off + i);
+  const int N = __ldg(p.t_off + i + 1) - o;
+  const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
+  uint32_t bad = 0;
+  if (N < 1 || N > Nmax) bad |= SV_DEV_BAD_KEEP_LEN;
+  if (!(T >= 0.0f) || isinf(T)) bad |= SV_DEV_BAD_TEMPERATURE;
+  const bool sampled = T > 0.0f;
+  if (!bad && (o < 0 || static_cast<int64_t>(o) + N > p.t_rows)) bad |= SV_DEV_BAD_OFFSETS;
+  if (!bad && sampled && N > 1 && p.draft == nullptr) bad |= SV_DEV_NO_DRAFT_ROWS;
+  if (tid == 0) {
+    ws.bad = 0;
+    ws.flags = 0;
+    ws.stop = 0;
+    ws.aborted = 0;
+    for (int s = 0; s < kWalkStages; ++s) mbar_init(&full_bar[s], 1);
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (!bad) {
+    for (int c = tid; c < N; c += kWalkThreads) {
+      const int pc = c == 0 ? -1 : __ldg(p.tree_parent + o + c);
+      const int tc = c == 0 ? -1 : __ldg(p.tree_tokens + o + c);
+      if (c > 0 && (pc < 0 || pc >= c)) atomicOr(&ws.bad, SV_DEV_BAD_PARENT);
+      if (c > 0 && (tc < 0 || tc >= p.V)) atomicOr(&ws.bad, SV_DEV_BAD_TOKEN);
+      par[c] = pc;
+      tokn[c] = tc;
+      first[c] = -1;
+    }
+  }
+  __syncthreads();
+  bad |= ws.bad;
+  if (bad) {
+    for (int j = tid; j < Nmax; j += kWalkThreads) {
+      out_path[j] = -1;
+      out_tok[j] = -1;
+    }
+    if (tid == 0) {
+      atomicOr(p.status, bad);
+      p.out_accept_len[i] = -1;
+      if (p.out_flags) p.out_flags[i] = SV_FLAG_INVALID;
+    }
+    return;
+  }
+  if (tid == 0) {  // children in increasing node order: insert from the last node down
+    for (int c = N - 1; c >= 1; --c) {
+      next[c] = first[par[c]];
+      first[par[c]] = c;
+    }
+  }
+  const float kscale = sampled ? kscale_of(T) : 0.0f;
+  const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
+  const ChunkRecord* recs = p.rec + static_cast<int64_t>(i) * R * NC;
+  float* mass = p.mass + static_cast<int64_t>(i) * NC * kDrawRanges;
+  __syncthreads();
+
+  uint32_t it = 0;  // ring stages consumed so far (every thread keeps the same count)
+  // One pass over a node's rows with weights w: the range sums (mass) and their total (ws.Z).
+  auto pass = [&](const char* trow, const char* drow, const Weights& w) {
+    auto issue = [&](int c, uint32_t k) {  // chunk c into ring slot k % kWalkStages (thread 0)
+      const int stage = k % kWalkStages;
+      unsigned char* sb = ring + static_cast<size_t>(stage) * 2 * kStageBytes;
+      const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+      const Split st = split_range<kElt>(trow, c0, len);
+      const Split sd = w.residual ? split_range<kElt>(drow, c0, len) : Split{0, 0, 0};
+      const uint32_t bytes = static_cast<uint32_t>(st.nvec + sd.nvec) * 16u;
+      if (bytes == 0) {
+        mbar_arrive(&full_bar[stage]);
+        return;
+      }
+      mbar_arrive_expect_tx(&full_bar[stage], bytes);
+      if (st.nvec) bulk_g2s(sb, trow + static_cast<int64_t>(c0 + st.head) * kElt, st.nvec * 16u, &full_bar[stage]);
+      if (sd.nvec)
+        bulk_g2s(sb + kStageBytes, drow + static_cast<int64_t>(c0 + sd.head) * kElt, sd.nvec * 16u, &full_bar[stage]);
+    };
+    if (tid == 0)
+      for (int c = 0; c < kWalkStages && c < NC; ++c) issue(c, it + c);
+    for (int c = 0; c < NC; ++c, ++it) {
+      const int stage = it % kWalkStages;
+      if (tid == 0 && !ws.aborted && !mbar_wait(&full_bar[stage], (it / kWalkStages) & 1u, p.status, p.wait_limit_ns))
+        ws.aborted = 1;
+      __syncthreads();
+      const unsigned char* sb = ring + static_cast<size_t>(stage) * 2 * kStageBytes;
+      const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+      const Split st = split_range<kElt>(trow, c0, len);
+      const Split sd = w.residual ? split_range<kElt>(drow, c0, len) : Split{0, 0, 0};
+      int lo, hi;
+      range_of(len, warp, &lo, &hi);
+      float sum = 0.0f;
+      for (int e = lo + lane; e < hi; e += 32) {
+        const float tx = staged<DT>(sb, trow, c0, e, st);
+        const float dx = w.residual ? staged<DT>(sb + kStageBytes, drow, c0, e, sd) : 0.0f;
+        sum += weight(tx, dx, w);
+      }
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o2);
+      if (lane == 0) mass[c * kDrawRanges + warp] = sum;
+      __syncthreads();  // the stage is read: it may be refilled
+      if (tid == 0 && !ws.aborted && c + kWalkStages < NC) issue(c + kWalkStages, it + kWalkStages);
+    }
+    __syncthreads();
+    if (warp == 0) {  // the total, in a fixed order
+      float z = 0.0f;
+      for (int e = lane; e < NC * kDrawRanges; e += 32) z += mass[e];
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o2);
+      if (lane == 0) ws.Z = z;
+    }
+    __syncthreads();
+  };
+
+  // Inverse-CDF pick over the weights of the last pass (total ws.Z) with uniform u: the crossing
+  // range (warp 0), then the entry inside it (warp 0 again, 32 entries at a time).  Sets ws.y.
+  auto pick = [&](const char* trow, const char* drow, const Weights& w, float u) {
+    if (warp == 0) {
+      const float thr = u * ws.Z;
+      float before = 0.0f;
+      // first range whose running sum exceeds thr (or the last with weight > 0)
+      float run = 0.0f, before_last = 0.0f;
+      int estar = -1, last_pos = -1;
+      const int NE = NC * kDrawRanges;
+      for (int j0 = 0; j0 < NE && estar < 0; j0 += 32) {
+        const int j = j0 + lane;
+        const float wj = j < NE ? mass[j] : 0.0f;
+        float incl = wj;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const float yv = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += yv;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < NE && wj > 0.0f && run + incl > thr);
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, j < NE && wj > 0.0f);
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          estar = j0 + src;
+          before = run + __shfl_sync(0xFFFFFFFFu, incl - wj, src);
+        } else if (pos) {
+          const int src = 31 - __clz(pos);
+          last_pos = j0 + src;
+          before_last = run + __shfl_sync(0xFFFFFFFFu, incl - wj, src);
+        }
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (estar < 0) {
+        estar = last_pos >= 0 ? last_pos : 0;
+        before = before_last;
+      }
+      // the entry inside range estar
+      const int c = estar / kDrawRanges, r = estar - c * kDrawRanges;
+      const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
+      int lo, hi;
+      range_of(len, r, &lo, &hi);
+      float run2 = before;
+      int y = -1, ylast = -1;
+      for (int e0 = lo; e0 < hi && y < 0; e0 += 32) {
+        const int e = e0 + lane;
+        float wv = 0.0f;
+        if (e < hi) wv = weight(load_logit<DT>(trow, c0 + e), w.residual ? load_logit<DT>(drow, c0 + e) : 0.0f, w);
+        float incl = wv;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const float yv = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += yv;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, e < hi && wv > 0.0f && run2 + incl > thr);
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, e < hi && wv > 0.0f);
+        if (hit) y = c0 + e0 + __ffs(hit) - 1;
+        else if (pos) ylast = c0 + e0 + 31 - __clz(pos);
+        run2 += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) ws.y = y >= 0 ? y : (ylast >= 0 ? ylast : c0 + lo);
+    }
+    __syncthreads();
+  };
+
+  // ---- the walk ----
+  int node = 0, L = 0;
+  for (int step = 0; step < N; ++step) {
+    const bool kids = first[node] >= 0;
+    // row statistics of the node (target row: warp 0; draft row: warp 1)
+    if (warp == 0) {
+      float m, s;
+      int g;
+      merge_row(recs + static_cast<int64_t>(node) * NC, NC, sampled, kscale, &m, &s, &g);
+      if (lane == 0) {
+        ws.mt = m;
+        ws.st = s;
+        ws.gt = g;
+      }
+    } else if (warp == 1 && sampled && kids) {
+      float m, s;
+      int g;
+      merge_row(recs + static_cast<int64_t>(p.Kmax + 1 + node) * NC, NC, true, kscale, &m, &s, &g);
+      if (lane == 0) {
+        ws.md = m;
+        ws.sd = s;
+      }
+    }
+    __syncthreads();
+    if (!sampled) {  // greedy: the first child holding the target argmax
+      const int g = ws.gt;
+      int acc = -1;
+      for (int c = first[node]; c >= 0; c = next[c])
+        if (tokn[c] == g) {
+          acc = c;
+          break;
+        }
+      if (acc < 0) {
+        if (tid == 0) ws.y = g;
+        break;
+      }
+      if (tid == 0) path[L] = acc;
+      ++L;
+      node = acc;
+      __syncthreads();
+      continue;
+    }
+    const char* trow = node_row<DT>(p.target, static_cast<int64_t>(o) + node, p.t_row_stride);
+    const char* drow = kids ? node_row<DT>(p.draft, static_cast<int64_t>(o) + node, p.d_row_stride) : trow;
+    Weights w;
+    w.kscale = kscale;
+    w.ct = exp_offset(ws.mt, kscale);
+    w.inv_st = __frcp_rn(ws.st);
+    w.cd = kids ? exp_offset(ws.md, kscale) : 0.0f;
+    const float inv_sd = kids ? __frcp_rn(ws.sd) : 0.0f;
+    const float u_draw = philox_uniform_f(p.seed, static_cast<uint32_t>(node), static_cast<uint32_t>(rid), 1u, p.round);
+    if (!kids) {  // a leaf: y ~ p
+      w.residual = false;
+      w.qs = 0.0f;
+      pass(trow, trow, w);
+      if (ws.aborted) break;
+      pick(trow, trow, w, u_draw);
+      break;
+    }
+    // the children in order; after each rejection the residual's normaliser (one pass)
+    float a = 0.0f, Nr = 1.0f, a_pass = -1.0f;  // a_pass: the a of the weights the last pass summed
+    int acc = -1;
+    for (int c = first[node]; c >= 0; c = next[c]) {
+      if (tid == 0) {
+        const int x = tokn[c];
+        const float pv = __fmul_rn(ex2_approx(__fmaf_rn(load_logit<DT>(trow, x), kscale, -w.ct)), w.inv_st);
+        const float qv = __fmul_rn(ex2_approx(__fmaf_rn(load_logit<DT>(drow, x), kscale, -w.cd)), inv_sd);
+        const float prv = __fdiv_rn(fmaxf(0.0f, __fmaf_rn(-a, qv, pv)), Nr);
+        const float u = philox_uniform_f(p.seed, static_cast<uint32_t>(c - 1), static_cast<uint32_t>(rid), 0u, p.round);
+        if (qv == 0.0f) ws.flags |= SV_FLAG_Q_ZERO;
+        ws.accept = u * qv < prv ? 1 : 0;
+      }
+      __syncthreads();
+      if (ws.accept) {
+        acc = c;
+        break;
+      }
+      const float a_next = a + Nr;
+      w.residual = true;
+      w.qs = __fmul_rn(a_next, inv_sd);
+      pass(trow, drow, w);
+      if (ws.aborted) break;
+      if (ws.Z > 0.0f) {
+        a = a_next;
+        Nr = ws.Z;
+        a_pass = a;
+      } else {  // residual mass 0 (not reachable in exact arithmetic): p' stays
+        if (tid == 0) ws.flags |= SV_FLAG_Z_ZERO;
+        a_pass = -1.0f;
+      }
+      __syncthreads();
+    }
+    if (ws.aborted) break;
+    if (acc >= 0) {
+      if (tid == 0) path[L] = acc;
+      ++L;
+      node = acc;
+      __syncthreads();
+      continue;
+    }
+    // every child rejected: y ~ max(0, p - a q), from the last pass's range sums when they are of a
+    w.residual = a > 0.0f;
+    w.qs = __fmul_rn(a, inv_sd);
+    if (a_pass != a) {
+      pass(trow, drow, w);
+      if (ws.aborted) break;
+    }
+    pick(trow, drow, w, u_draw);
+    break;
+  }
+  __syncthreads();
+  // ---- outputs ----
+  for (int j = tid; j < Nmax; j += kWalkThreads) {
+    int pj = -1, tj = -1;
+    if (j < L) {
+      pj = path[j];
+      tj = tokn[pj];
+    } else if (j == L) {
+      tj = ws.aborted ? -1 : ws.y;
+    }
+    out_path[j] = pj;
+    out_tok[j] = tj;
+  }
+  if (tid == 0) {
+    p.out_accept_len[i] = L;
+    if (p.out_flags) p.out_flags[i] = static_cast<uint8_t>(ws.flags);
+  }
+}
+
+size_t walk_smem_bytes(int Nmax) {
+  return static_cast<size_t>(kWalkStages) * 2 * kStageBytes + 5 * sizeof(int) * static_cast<size_t>(Nmax);
+}
+
+std::mutex g_tree_mu;
+bool g_tree_ready[64][2] = {};
+
+template <int DT>
+cudaError_t launch_walk_t(const VerifyParams& p, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_tree_mu);
+    if (!g_tree_ready[dev][DT == SV_BF16 ? 0 : 1]) {
+      if ((e = cudaFuncSetAttribute(tree_walk_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(walk_smem_bytes(SV_MAX_DRAFT + 1)))) != cudaSuccess)
+        return e;
+      g_tree_ready[dev][DT == SV_BF16 ? 0 : 1] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B, 1, 1);
+  cfg.blockDim = dim3(kWalkThreads, 1, 1);
+  cfg.dynamicSmemBytes = walk_smem_bytes(p.Kmax + 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = prof_enabled() ? 0 : 1;
+  prof_before(SV_KERNEL_TREE_WALK, stream);
+  e = cudaLaunchKernelEx(&cfg, tree_walk_kernel<DT>, p);
+  prof_after(SV_KERNEL_TREE_WALK, stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_tree(const VerifyParams& p, sv_dtype dt, void* stream) {
+  const int e = launch_stats(p, dt, stream);
+  if (e != 0) return e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return static_cast<int>(dt == SV_BF16 ? launch_walk_t<SV_BF16>(p, s) : launch_walk_t<SV_F32>(p, s));
+}
+
+}  // namespace sv

@@ -99,16 +99,18 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
 // ------------------------------------------------------------------------------------------
 __device__ uint16_t request_info(const VerifyParams& p, int i, uint32_t* bad_out) {
   // every load is issued before any is used (one round trip)
-  const int n = p.keep_len ? __ldg(p.keep_len + i) : p.Kmax;
   const float T = p.temperature ? __ldg(p.temperature + i) : 0.0f;
   const int ta = p.t_off ? __ldg(p.t_off + i) : 0, tb = p.t_off ? __ldg(p.t_off + i + 1) : 0;
   const int da = p.d_off ? __ldg(p.d_off + i) : 0, dbb = p.d_off ? __ldg(p.d_off + i + 1) : 0;
+  // a tree of N nodes streams N target rows and (sampled) the draft rows of nodes 0..N-2 (node
+  // N - 1 is a leaf): the rows of a chain of N - 1 positions
+  const int n = p.tree ? tb - ta - 1 : (p.keep_len ? __ldg(p.keep_len + i) : p.Kmax);
   uint32_t bad = 0;
   if (n < 0 || n > p.Kmax) bad |= SV_DEV_BAD_KEEP_LEN;
   if (!(T >= 0.0f) || isinf(T)) bad |= SV_DEV_BAD_TEMPERATURE;
   const bool sampled = T > 0.0f;
-  const bool need_draft = (sampled || p.tokens == nullptr) && n > 0;  // n == 0: bonus row only
-  if (sampled && n > 0 && p.tokens == nullptr) bad |= SV_DEV_BAD_TOKEN;
+  const bool need_draft = (sampled || (p.tokens == nullptr && !p.tree)) && n > 0;  // n == 0: bonus row only
+  if (sampled && n > 0 && p.tokens == nullptr && !p.tree) bad |= SV_DEV_BAD_TOKEN;
   if (need_draft && p.draft == nullptr) bad |= SV_DEV_NO_DRAFT_ROWS;
   if (!bad && p.t_off &&
       (tb - ta < n + 1 || ta < 0 || (p.t_rows >= 0 && static_cast<int64_t>(ta) + n + 1 > p.t_rows)))
@@ -586,9 +588,6 @@ constexpr size_t kFinMaxStagedBytes = 48 * 1024;  // chunk records staged in sha
 constexpr int kFinMaxDynSmem = 96 * 1024;
 constexpr int kCombineThreads = 256, kCombineWarps = kCombineThreads / 32;
 constexpr int kMassThreads = 256, kMassWarps = kMassThreads / 32;
-// Each vocabulary chunk's draw weights are summed in kDrawRanges contiguous ranges (one per
-// warp); the pick kernel finds the crossing range and scans only that range.
-constexpr int kDrawRanges = 8;
 static_assert(kCombineWarps == kDrawRanges && kMassWarps == kDrawRanges, "one draw range per warp");
 // Requests with at most this many chunk records (rows x chunks) get their draw weights summed by
 // the combine kernel's CTAs, which each merge the request's records again; longer requests use
@@ -1209,7 +1208,7 @@ cudaError_t launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream
 }
 
 template <int DT>
-cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
+cudaError_t launch_row_stats_t(const VerifyParams& p, cudaStream_t stream) {
   const size_t table =
       p.uniform_rows > 0 ? 0 : static_cast<size_t>((p.B + 4) & ~3) * 4 + ((static_cast<size_t>(p.B) * 2 + 15) & ~size_t(15));
   const size_t dyn = static_cast<size_t>(StreamShape<DT>::kStages) * kStageBytes + table;
@@ -1229,7 +1228,13 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
   prof_before(SV_KERNEL_ROW_STATS, stream);
   row_stats_kernel<DT><<<grid, kStatsThreads, dyn, stream>>>(p);
   prof_after(SV_KERNEL_ROW_STATS, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t stream) {
+  cudaError_t e;
+  if ((e = launch_row_stats_t<DT>(p, stream)) != cudaSuccess) return e;
 
   const size_t csmem = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
   if ((e = launch_pdl(combine_kernel<DT>, dim3(p.fuse_draw ? p.nchunks : 1, p.B), kCombineThreads, csmem, stream,
@@ -1276,6 +1281,11 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
   off = align256(off + sizeof(ChunkRecord) * B * R * static_cast<size_t>(nchunks));
   L.total = off;
   return L;
+}
+
+int launch_stats(const VerifyParams& p, sv_dtype dt, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return static_cast<int>(dt == SV_BF16 ? launch_row_stats_t<SV_BF16>(p, s) : launch_row_stats_t<SV_F32>(p, s));
 }
 
 int launch_verify(const VerifyParams& p_in, sv_dtype dt, bool sampled, void* stream) {

@@ -117,3 +117,58 @@ def compare(orc, tok, alen, p=None, q=None, keep_len=None, temps=None, requests=
     print(f"parity: {len(idx)} requests compared, {near} excused at a near-boundary decision (cap {cap})")
     assert near <= cap, (near, cap)
     return near
+
+
+# ------------------------------------------------------------------ trees
+
+def run_tree(b, ws=None):
+    """Run sv_verify_tree on a synth TreeBatch; returns numpy (path, tokens, accept_len, flags)."""
+    out = sv.verify_tree(dev_rows(b.target, b.dtype), dev_rows(b.draft, b.dtype), i32(b.node_offsets), i32(b.parent),
+                         i32(b.tokens), f32(b.temperature), b.Nmax, seed=b.seed, round_=b.round,
+                         request_ids=i32(b.request_ids), ws=ws)
+    torch.cuda.synchronize()
+    return tuple(o.cpu().numpy() for o in out)
+
+
+def oracle_tree(b):
+    from oracle.tree import verify_tree_batch
+    return verify_tree_batch(b.target, b.draft, b.node_offsets, b.parent, b.tokens, b.temperature, b.seed, b.round,
+                             b.request_ids, b.dtype)
+
+
+def compare_tree(orc, path, tok, alen, b, requests=None, max_near=None):
+    """Paths, emitted tokens and accepted lengths bit-exact up to the first near-boundary decision
+    the oracle reports: an accept test of child c within 1e-6 of its threshold (the path must agree
+    up to c's parent), or a pick within 1e-6 Z of a bin edge (the path must agree; the drawn token
+    is free).  Excused requests are bounded by lam + 4 sqrt(lam) + 2, lam = sum over sampled requests
+    of V * 2e-6 + 2e-6 per node (an upper bound of the band's probability), unless max_near is given.
+    Returns the number excused."""
+    idx = list(range(b.B) if requests is None else requests)
+    near = 0
+    lam = 0.0
+    for i in idx:
+        r = orc[i]
+        L = len(r["path"])
+        N = b.nodes(i)
+        if float(b.temperature[i]) > 0.0:
+            lam += b.V * 2 * NEAR_TOL + 2 * NEAR_TOL * N
+        if r["near"] is None:
+            assert alen[i] == L, (i, alen[i], L)
+            assert list(path[i, :L]) == r["path"], (i, path[i, :L], r["path"])
+            assert list(tok[i, :L + 1]) == r["tokens"], (i, tok[i, :L + 1], r["tokens"])
+            assert np.all(path[i, L:] == -1) and np.all(tok[i, L + 1:] == -1), i
+            continue
+        near += 1
+        kind, where = r["near"]
+        if kind == NEAR_PICK:
+            assert alen[i] == L and list(path[i, :L]) == r["path"], (i, path[i, :L], r["path"])
+            assert list(tok[i, :L]) == r["tokens"][:L], i
+        else:  # an accept test of child `where`: everything decided before it agrees
+            pc = int(b.parent[b.node_offsets[i] + where])  # the walk reached pc before testing `where`
+            pre = [] if pc == 0 else r["path"][: r["path"].index(pc) + 1]
+            k = len(pre)
+            assert list(path[i, :k]) == pre, (i, path[i, :k], pre)
+    cap = max_near if max_near is not None else int(lam + 4.0 * np.sqrt(lam) + 2.0)
+    print(f"tree parity: {len(idx)} requests compared, {near} excused at a near-boundary decision (cap {cap})")
+    assert near <= cap, (near, cap)
+    return near
