@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from synth import workloads as W  # noqa: E402
+from synth import trees as TR  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -41,6 +42,7 @@ WORKLOADS = {
     "c3": "block-parallel DFly-style verify T=0.6, B=64 K=16 V=151936 fp32",
     "c4": "D-cut schedule (B=64 D=16 budget 384, c=1+0.05K) + ragged verify T=1.0 V=151936 bf16",
     "c5": "mixed round c64: 32 chat K=3 + 32 code K=16, T in {0,0.6,1}, V=151936 bf16",
+    "t1": "token-tree verify T=1.0, B=64 trees of 16 nodes (8 shapes, 15 candidates each), V=151936 bf16",
 }
 
 
@@ -61,12 +63,16 @@ def make_sets(workload: str, n_sets: int, base_seed: int):
             sets.append({"batch": b, "sched": s})
         elif workload == "c5":
             sets.append({"batch": W.c5_mixed(seed=base_seed, rnd=j)})
+        elif workload == "t1":
+            sets.append({"batch": TR.t1_tree(seed)})
     return sets
 
 
 def algorithmic_bytes(b, keep_len) -> int:
     """Each needed logit byte once: n_i + 1 target rows, plus n_i draft rows when the request
-    samples (T > 0) or takes its drafted tokens from the draft argmax."""
+    samples (T > 0) or takes its drafted tokens from the draft argmax.  A tree of N nodes counts
+    as n = N - 1: N target rows and, sampled, the draft rows of the N - 1 nodes that can have
+    children (the walk's re-reads of a node's rows after a rejection are not counted)."""
     elt = 2 if b.dtype == "bf16" else 4
     rows = 0
     for i in range(b.B):
@@ -202,16 +208,27 @@ class GpuWorkload:
         self.sets = []
         b0 = sets[0]["batch"]
         self.dt = sv.SV_BF16 if b0.dtype == "bf16" else sv.SV_F32
-        self.B, self.Kmax, self.V = b0.B, b0.Kmax, b0.V
-        self.ws = sv.workspace(sv.SV_OP_VERIFY, self.B, self.Kmax, self.V, self.dt, device)
+        self.tree = workload == "t1"
+        self.B, self.V = b0.B, b0.V
+        self.Kmax = b0.Nmax if self.tree else b0.Kmax  # trees: Nmax
+        self.ws = sv.workspace(sv.SV_OP_TREE if self.tree else sv.SV_OP_VERIFY, self.B, self.Kmax, self.V, self.dt,
+                               device)
         self.ws_sched = sv.workspace(sv.SV_OP_SCHEDULE, self.B, self.Kmax, 1, sv.SV_F32, device)
         for s in sets:
             self.sets.append(self._upload(s))
-        self.out = (torch.empty((self.B, self.Kmax + 1), dtype=torch.int32, device=device),
-                    torch.empty(self.B, dtype=torch.int32, device=device),
-                    torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
-                    torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
-                    torch.empty(self.B, dtype=torch.uint8, device=device))
+        if self.tree:
+            self.out = (torch.empty((self.B, self.Kmax), dtype=torch.int32, device=device),
+                        torch.empty((self.B, self.Kmax), dtype=torch.int32, device=device),
+                        torch.empty(self.B, dtype=torch.int32, device=device),
+                        torch.empty(self.B, dtype=torch.uint8, device=device))
+        else:
+            self.out = (torch.empty((self.B, self.Kmax + 1), dtype=torch.int32, device=device),
+                        torch.empty(self.B, dtype=torch.int32, device=device),
+                        torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
+                        torch.empty((self.B, self.Kmax), dtype=torch.float32, device=device),
+                        torch.empty(self.B, dtype=torch.uint8, device=device))
+        # what a caller reads back: emitted tokens and accepted lengths
+        self.results = (self.out[1], self.out[2]) if self.tree else (self.out[0], self.out[1])
         self.sched_out = (torch.empty(self.B, dtype=torch.int32, device=device),
                           torch.empty(self.B + 1, dtype=torch.int32, device=device),
                           torch.empty(1, dtype=torch.int32, device=device),
@@ -227,6 +244,10 @@ class GpuWorkload:
 
     def _upload(self, s):
         b = s["batch"]
+        if self.tree:
+            return {"b": b, "target": self._t(b.target, b.dtype), "draft": self._t(b.draft, b.dtype),
+                    "t_off": self._t(b.node_offsets), "parent": self._t(b.parent), "tokens": self._t(b.tokens),
+                    "temp": self._t(b.temperature), "rid": self._t(b.request_ids)}
         d = {"b": b,
              "target": self._t(b.target, b.dtype), "draft": self._t(b.draft, b.dtype),
              "t_off": self._t(b.t_offsets), "d_off": self._t(b.d_offsets),
@@ -241,7 +262,11 @@ class GpuWorkload:
         sv = self.sv
         d = self.sets[j % len(self.sets)]
         b = d["b"]
-        if self.workload == "c1":
+        if self.tree:
+            sv.sv_verify_tree(d["target"], b.V, d["draft"], b.V, d["t_off"], b.target.shape[0], d["parent"],
+                              d["tokens"], d["temp"], b.seed, b.round, d["rid"], self.dt, self.B, self.Kmax, self.V,
+                              *self.out, self.ws, stream)
+        elif self.workload == "c1":
             sv.sv_verify_greedy(d["target"], b.V, d["draft"], b.V, None, self.dt, self.B, self.Kmax, self.V,
                                 self.out[0], self.out[1], self.ws, stream)
         elif self.workload in ("c2", "c3"):
@@ -565,11 +590,10 @@ def run_e2e(gw, warm, steps, stream):
     import torch
     sv = gw.sv
     pinned = []
-    names = ("target", "draft", "t_off", "d_off", "tokens", "keep", "temp", "rid", "alpha")
+    names = ("target", "draft", "t_off", "d_off", "parent", "tokens", "keep", "temp", "rid", "alpha")
     for d in gw.sets[:2]:
         pinned.append({k: d[k].cpu().pin_memory() for k in names if d.get(k) is not None})
-    h_out = [torch.empty(tuple(gw.out[0].shape), dtype=torch.int32).pin_memory(),
-             torch.empty(tuple(gw.out[1].shape), dtype=torch.int32).pin_memory()]
+    h_out = [torch.empty(tuple(r.shape), dtype=torch.int32).pin_memory() for r in gw.results]
     # device staging buffers for one set (the step's inputs land here every step)
     stage = {k: torch.empty_like(gw.sets[0][k]) for k in pinned[0]}
     h2d = sum(v.numel() * v.element_size() for v in pinned[0].values())
@@ -585,8 +609,8 @@ def run_e2e(gw, warm, steps, stream):
         d.update(stage)
         gw.sets = [d]
         gw.step(0)
-        h_out[0].copy_(gw.out[0], non_blocking=True)
-        h_out[1].copy_(gw.out[1], non_blocking=True)
+        for h, r in zip(h_out, gw.results):
+            h.copy_(r, non_blocking=True)
 
     for j in range(2):
         one(j)
@@ -626,6 +650,13 @@ def oracle_step(workload, sets, j, req_slice):
     from oracle.schedule import dcut_schedule
     s = sets[j % len(sets)]
     b = s["batch"]
+    if workload == "t1":
+        from oracle.tree import verify_tree_batch
+        lo, hi = req_slice
+        o = b.node_offsets
+        verify_tree_batch(b.target, b.draft, o[lo:hi + 1], b.parent, b.tokens, b.temperature[lo:hi], b.seed, b.round,
+                          b.request_ids[lo:hi], b.dtype)
+        return int(np.sum(b.keep_len[lo:hi]))
     keep = b.keep_len
     if workload == "c4":
         sc = s["sched"]
@@ -753,7 +784,7 @@ def main():
     ap.add_argument("--impl", default="sv", choices=["sv", "reference"])
     ap.add_argument("--workload", default="c3", choices=sorted(WORKLOADS),
                     help="headline workload (default c3, the largest stream)")
-    ap.add_argument("--also", default="c2,c4,c5",
+    ap.add_argument("--also", default="c2,c4,c5,t1",
                     help="comma-separated workloads measured after the headline and reported under "
                          "other_workloads ('' for none)")
     args = ap.parse_args()

@@ -13,7 +13,11 @@
 //     = max(0, p - (a + N) q) / N).  So a rejection costs one pass over the node's target and draft
 //     rows, which sums the weights in 8 ranges per vocabulary chunk; the pass after the last
 //     rejection also serves the draw: the crossing range among the range sums, then a scan of it.
-// The passes stream the two rows through a 4-stage ring of 1-D bulk copies (cp.async.bulk).
+// A request's walk runs on a cluster of 8 CTAs: every CTA takes the same decisions (same records,
+// same logits, same Philox uniforms), and each pass is split across them by vocabulary chunk, each
+// CTA streaming its chunks of the two rows through a 2-stage ring of 1-D bulk copies
+// (cp.async.bulk); the range sums meet in the workspace behind cluster barriers, and every CTA
+// adds them up in the same order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,7 +34,8 @@ namespace {
 constexpr float kLog2eF = 1.44269504088896340736f;
 constexpr int kWalkThreads = 256;
 constexpr int kWalkWarps = kWalkThreads / 32;
-constexpr int kWalkStages = 4;  // ring of (target chunk, draft chunk) pairs
+constexpr int kWalkStages = 2;  // ring of (target chunk, draft chunk) pairs
+constexpr int kCluster = 8;     // CTAs per request (a thread-block cluster)
 static_assert(kWalkWarps == kDrawRanges, "one draw range of a chunk per warp");
 
 __device__ __forceinline__ float kscale_of(float T) { return __fdiv_rn(kLog2eF, T); }
@@ -142,6 +147,12 @@ __device__ __forceinline__ float weight(float tx, float dx, const Weights& w) {
   return fmaxf(0.0f, __fmaf_rn(pv, w.inv_st, -ex2_approx(__fmaf_rn(dx, w.kscale, -w.cd)) * w.qs));
 }
 
+// Barrier of every thread of the cluster; orders the memory accesses before it (release) before
+// those after it (acquire) across the cluster's CTAs.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 struct WalkSmem {
   float mt, st, md, sd;  // row statistics of the current node
   int gt;
@@ -169,7 +180,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   pdl_wait();  // the streaming kernel's records are complete
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x;
+  const int i = blockIdx.x / kCluster, crank = blockIdx.x % kCluster;  // request, rank in its cluster
   const int NC = p.nchunks, R = 2 * p.Kmax + 1;
   int32_t* out_path = p.out_path + static_cast<int64_t>(i) * Nmax;
   int32_t* out_tok = p.out_tokens + static_cast<int64_t>(i) * Nmax;
@@ -206,15 +217,17 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   }
   __syncthreads();
   bad |= ws.bad;
-  if (bad) {
-    for (int j = tid; j < Nmax; j += kWalkThreads) {
-      out_path[j] = -1;
-      out_tok[j] = -1;
-    }
-    if (tid == 0) {
-      atomicOr(p.status, bad);
-      p.out_accept_len[i] = -1;
-      if (p.out_flags) p.out_flags[i] = SV_FLAG_INVALID;
+  if (bad) {  // the same in every CTA of the cluster: the first one reports it
+    if (crank == 0) {
+      for (int j = tid; j < Nmax; j += kWalkThreads) {
+        out_path[j] = -1;
+        out_tok[j] = -1;
+      }
+      if (tid == 0) {
+        atomicOr(p.status, bad);
+        p.out_accept_len[i] = -1;
+        if (p.out_flags) p.out_flags[i] = SV_FLAG_INVALID;
+      }
     }
     return;
   }
@@ -228,6 +241,10 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
   const ChunkRecord* recs = p.rec + static_cast<int64_t>(i) * R * NC;
   float* mass = p.mass + static_cast<int64_t>(i) * NC * kDrawRanges;
+  // a wait that ran out in any CTA of the cluster (set before a cluster barrier, read after it);
+  // cleared before the first barrier
+  uint32_t* abort_word = reinterpret_cast<uint32_t*>(p.req + i);
+  if (crank == 0 && tid == 0) *abort_word = 0;
   __syncthreads();
 
   uint32_t it = 0;  // ring stages consumed so far (every thread keeps the same count)
@@ -249,9 +266,13 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
       if (sd.nvec)
         bulk_g2s(sb + kStageBytes, drow + static_cast<int64_t>(c0 + sd.head) * kElt, sd.nvec * 16u, &full_bar[stage]);
     };
+    cluster_sync();  // every CTA has added up the previous pass's sums: they may be overwritten
+    // this CTA's chunks: crank, crank + kCluster, ...
+    const int nloc = crank < NC ? (NC - 1 - crank) / kCluster + 1 : 0;
     if (tid == 0)
-      for (int c = 0; c < kWalkStages && c < NC; ++c) issue(c, it + c);
-    for (int c = 0; c < NC; ++c, ++it) {
+      for (int k = 0; k < kWalkStages && k < nloc; ++k) issue(crank + k * kCluster, it + k);
+    for (int k = 0; k < nloc; ++k, ++it) {
+      const int c = crank + k * kCluster;
       const int stage = it % kWalkStages;
       if (tid == 0 && !ws.aborted && !mbar_wait(&full_bar[stage], (it / kWalkStages) & 1u, p.status, p.wait_limit_ns))
         ws.aborted = 1;
@@ -272,12 +293,16 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
       for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o2);
       if (lane == 0) mass[c * kDrawRanges + warp] = sum;
       __syncthreads();  // the stage is read: it may be refilled
-      if (tid == 0 && !ws.aborted && c + kWalkStages < NC) issue(c + kWalkStages, it + kWalkStages);
+      if (tid == 0 && !ws.aborted && k + kWalkStages < nloc)
+        issue(crank + (k + kWalkStages) * kCluster, it + kWalkStages);
     }
+    if (tid == 0 && ws.aborted) atomicOr(abort_word, 1u);
     __syncthreads();
-    if (warp == 0) {  // the total, in a fixed order
+    cluster_sync();  // every CTA's range sums (and any wait that ran out) are written
+    if (tid == 0) ws.aborted = __ldcg(abort_word) != 0u ? 1 : 0;  // the same in every CTA
+    if (warp == 0) {  // the total, in a fixed order (the same in every CTA)
       float z = 0.0f;
-      for (int e = lane; e < NC * kDrawRanges; e += 32) z += mass[e];
+      for (int e = lane; e < NC * kDrawRanges; e += 32) z += __ldcg(mass + e);
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o2);
       if (lane == 0) ws.Z = z;
@@ -288,7 +313,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   // Inverse-CDF pick over the weights of the last pass (total ws.Z) with uniform u: the crossing
   // range (warp 0), then the entry inside it (warp 0 again, 32 entries at a time).  Sets ws.y.
   auto pick = [&](const char* trow, const char* drow, const Weights& w, float u) {
-    if (warp == 0) {
+    if (warp == 0 && crank == 0) {  // the walk ends here: one CTA of the cluster draws
       const float thr = u * ws.Z;
       float before = 0.0f;
       // first range whose running sum exceeds thr (or the last with weight > 0)
@@ -297,7 +322,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
       const int NE = NC * kDrawRanges;
       for (int j0 = 0; j0 < NE && estar < 0; j0 += 32) {
         const int j = j0 + lane;
-        const float wj = j < NE ? mass[j] : 0.0f;
+        const float wj = j < NE ? __ldcg(mass + j) : 0.0f;
         float incl = wj;
 #pragma unroll
         for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -460,6 +485,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
     break;
   }
   __syncthreads();
+  if (crank != 0) return;  // one CTA of the cluster writes the outputs
   // ---- outputs ----
   for (int j = tid; j < Nmax; j += kWalkThreads) {
     int pj = -1, tj = -1;
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   }
 }
 
-size_t walk_smem_bytes(int Nmax) {
+size_t walk_smem_bytes(int Nmax) {  // the ring, then five int arrays of Nmax
   return static_cast<size_t>(kWalkStages) * 2 * kStageBytes + 5 * sizeof(int) * static_cast<size_t>(Nmax);
 }
 
@@ -501,15 +527,19 @@ cudaError_t launch_walk_t(const VerifyParams& p, cudaStream_t stream) {
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B, 1, 1);
+  cfg.gridDim = dim3(p.B * kCluster, 1, 1);
   cfg.blockDim = dim3(kWalkThreads, 1, 1);
   cfg.dynamicSmemBytes = walk_smem_bytes(p.Kmax + 1);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = prof_enabled() ? 0 : 1;
+  cfg.numAttrs = prof_enabled() ? 1 : 2;
   prof_before(SV_KERNEL_TREE_WALK, stream);
   e = cudaLaunchKernelEx(&cfg, tree_walk_kernel<DT>, p);
   prof_after(SV_KERNEL_TREE_WALK, stream);

@@ -50,6 +50,11 @@ class TreeBatch:
     def nodes(self, i: int) -> int:
         return int(self.node_offsets[i + 1] - self.node_offsets[i])
 
+    @property
+    def keep_len(self) -> np.ndarray:
+        """Drafted candidates per request (every node but the root)."""
+        return (np.diff(self.node_offsets) - 1).astype(np.int32)
+
 
 def tree_shape(branch: list[int], max_nodes: int) -> np.ndarray:
     """Parent array of a breadth-first tree: level-l nodes get branch[l] children each, until

@@ -136,22 +136,45 @@ def oracle_tree(b):
                              b.request_ids, b.dtype)
 
 
+def expected_excused_tree(b, orc, i) -> float:
+    """Expected near-boundary excusals of tree request i, without the oracle's band code: the draw's
+    weights rebuilt with scipy's softmax at the node where the oracle's walk stopped (p, or the
+    residual after every child there was rejected: p' = norm(max(0, p' - q)) per child), then
+    sum_v min(r_v / Z, 2 NEAR_TOL), plus 2 NEAR_TOL per accept test."""
+    from scipy.special import softmax
+    T = float(np.float32(b.temperature[i]))
+    if not T > 0.0:
+        return 0.0
+    o, N = int(b.node_offsets[i]), b.nodes(i)
+    par = b.parent[o:o + N]
+    path = orc[i]["path"]
+    node = path[-1] if path else 0
+    P = softmax(_decode(b.target[o + node], b.dtype) / T)
+    r = P
+    kids = [c for c in range(1, N) if par[c] == node]
+    if kids:
+        Q = softmax(_decode(b.draft[o + node], b.dtype) / T)
+        pr = P
+        for _ in kids:
+            res = np.maximum(0.0, pr - Q)
+            if res.sum() > 0.0:
+                r, pr = res, res / res.sum()
+    return float(np.minimum(r / r.sum(), 2 * NEAR_TOL).sum()) + 2 * NEAR_TOL * N
+
+
 def compare_tree(orc, path, tok, alen, b, requests=None, max_near=None):
     """Paths, emitted tokens and accepted lengths bit-exact up to the first near-boundary decision
     the oracle reports: an accept test of child c within 1e-6 of its threshold (the path must agree
     up to c's parent), or a pick within 1e-6 Z of a bin edge (the path must agree; the drawn token
-    is free).  Excused requests are bounded by lam + 4 sqrt(lam) + 2, lam = sum over sampled requests
-    of V * 2e-6 + 2e-6 per node (an upper bound of the band's probability), unless max_near is given.
-    Returns the number excused."""
+    is free).  Excused requests are bounded by lam + 4 sqrt(lam) + 2 with lam the sum of
+    expected_excused_tree, unless max_near is given.  Returns the number excused."""
     idx = list(range(b.B) if requests is None else requests)
     near = 0
     lam = 0.0
     for i in idx:
         r = orc[i]
         L = len(r["path"])
-        N = b.nodes(i)
-        if float(b.temperature[i]) > 0.0:
-            lam += b.V * 2 * NEAR_TOL + 2 * NEAR_TOL * N
+        lam += expected_excused_tree(b, orc, i)
         if r["near"] is None:
             assert alen[i] == L, (i, alen[i], L)
             assert list(path[i, :L]) == r["path"], (i, path[i, :L], r["path"])
