@@ -36,11 +36,13 @@ def _rng(*key: int) -> np.random.Generator:
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest, ties to even); return uint16 bits."""
+    """Round float32 to bfloat16 (nearest, ties to even); return uint16 bits.  In 32-bit integer
+    arithmetic: bits + 0x7FFF + lsb cannot wrap for a non-NaN float (the largest, -inf, is
+    0xFF800000), and NaNs are set apart."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    lsb = (b >> np.uint64(16)) & np.uint64(1)
-    r = (b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    b = x.view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + (np.uint32(0x7FFF) + lsb)) >> np.uint32(16)
     # keep NaN a NaN (never produced by the recipes, but be safe)
     nan = np.isnan(x)
     out = r.astype(np.uint16)
