@@ -1255,6 +1255,9 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
 
 }  // namespace
 
+// Vocabulary chunks of at most one 16 KB stage.  bf16 rows are cut into full stages (and one short
+// chunk at the end), which the stream reduces without predicates (an A/B on GB300: C5 75.8 -> 73.8
+// us per step against equal chunks of 8000); fp32 rows into equal chunks.
 void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks) {
   const int elt = dt == SV_BF16 ? 2 : 4;
   const int vec = 16 / elt;
@@ -1263,7 +1266,7 @@ void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks) {
   if (nc < 1) nc = 1;
   int cl = (V + nc - 1) / nc;
   cl = (cl + vec - 1) / vec * vec;
-  if (cl > stage_elems) cl = stage_elems;
+  if (cl > stage_elems || (dt == SV_BF16 && nc > 1)) cl = stage_elems;
   *chunk_len = cl;
   *nchunks = (V + cl - 1) / cl;
 }
