@@ -161,12 +161,6 @@ __device__ __forceinline__ float weight(float tx, float dx, const Weights& w) {
   return fmaxf(0.0f, __fmaf_rn(pv, w.inv_st, -ex2_approx(__fmaf_rn(dx, w.kscale, -w.cd)) * w.qs));
 }
 
-// Barrier of every thread of the cluster; orders the memory accesses before it (release) before
-// those after it (acquire) across the cluster's CTAs.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 struct WalkSmem {
   float mt, st, md, sd;  // row statistics of the current node
   int gt;
