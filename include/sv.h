@@ -191,6 +191,54 @@ sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32
                            size_t ws_bytes, void* stream);
 
 /*
+ * Vocabulary-parallel verification (the LM head split across GPUs by vocabulary
+ * columns, as in the pages' TP = 8 serving: [explainer] "The numbers", [release]
+ * "Key Takeaways").  sv_verify_sample is four steps, and every step but the
+ * accept chain is a sum or a search over the vocabulary in fixed chunks
+ * (sv_vocab_chunks).  With the chunks split into contiguous ranges, one per
+ * GPU, each GPU runs:
+ *   SV_PHASE_STATS    its chunks of every row  -> chunk records (workspace)
+ *   (all-gather of the records region: every GPU then holds every chunk's record)
+ *   SV_PHASE_ACCEPT   the accept chain from all records: identical p, q, accepted
+ *                     prefixes and draw state on every GPU
+ *   SV_PHASE_WEIGHTS  its chunks' draw-weight range sums (workspace)
+ *   (all-gather of the two range-sum regions)
+ *   SV_PHASE_PICK     the crossing range from all range sums; only the GPU whose
+ *                     chunks hold it writes the drawn token (out_tokens[i][a]) and
+ *                     the Z_ZERO flag; the others leave them (initialise the token
+ *                     to -1 and take the maximum across GPUs)
+ * Results match sv_verify_sample's: the same chunk arithmetic, with the sums
+ * grouped at the shard boundaries (a chunk record merges the chunks one CTA
+ * streams in a row), so p and q agree to float32 rounding and the decisions
+ * agree outside the near-boundary band.  sv_verify_regions gives the regions' workspace offsets: records are
+ * [B][2K+1][nchunks] ChunkRecords of 16 bytes (a GPU's chunks are a contiguous
+ * run of every (request, row)), range sums [B][nchunks][8] floats in two arrays.
+ */
+enum { SV_PHASE_STATS = 0, SV_PHASE_ACCEPT = 1, SV_PHASE_WEIGHTS = 2, SV_PHASE_PICK = 3 };
+
+/* The vocabulary tiling of the verification kernels: nchunks chunks of chunk_len
+ * entries (the last may be shorter). */
+sv_status sv_vocab_chunks(int V, sv_dtype dt, int* chunk_len, int* nchunks);
+
+/* Workspace offsets and sizes (bytes) of the chunk records and of the two
+ * range-sum arrays of a verification workspace for (B, K, V, dt). */
+sv_status sv_verify_regions(int B, int K, int V, sv_dtype dt, size_t* rec_offset, size_t* rec_bytes,
+                            size_t* mass_offset, size_t* mass_p_offset, size_t* mass_bytes);
+
+/* One step of sv_verify_sample over the vocabulary chunks [c_begin, c_end)
+ * (0 <= c_begin < c_end <= nchunks).  Arguments as sv_verify_sample, except
+ * that target / draft address the GPU's own columns: entry v of a row (v in
+ * [c_begin, c_end) chunks) is at row + (v - c_begin * chunk_len).  STATS and
+ * WEIGHTS read logits; ACCEPT and PICK read the workspace (PICK also reads the
+ * crossing range's logits on the GPU that holds them). */
+sv_status sv_verify_sample_phase(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                                 const int32_t* draft_tokens, const float* temperature, uint64_t seed,
+                                 uint32_t round, const int32_t* request_ids, sv_dtype dt, int B, int K, int V,
+                                 int c_begin, int c_end, int phase, int32_t* out_tokens, int32_t* out_accept_len,
+                                 float* out_p, float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/*
  * sv_verify_tree -- multi-candidate (token tree) verification by multi-step
  * speculative sampling (Miao et al., "SpecInfer", ASPLOS 2024, section 4.2);
  * a chain-shaped tree is exactly sv_verify_ragged ([explainer] "DFly": the

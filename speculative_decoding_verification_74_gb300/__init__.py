@@ -27,6 +27,7 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, S
 SV_BF16, SV_F32 = 0, 1
 SV_OP_VERIFY, SV_OP_SCHEDULE, SV_OP_TREE = 0, 1, 2
 SV_OBJ_THROUGHPUT, SV_OBJ_NET = 0, 1
+SV_PHASE_STATS, SV_PHASE_ACCEPT, SV_PHASE_WEIGHTS, SV_PHASE_PICK = range(4)
 (SV_DEV_BAD_TOKEN, SV_DEV_BAD_TEMPERATURE, SV_DEV_BAD_KEEP_LEN, SV_DEV_BAD_OFFSETS, SV_DEV_NO_DRAFT_ROWS,
  SV_DEV_BAD_ALPHA, SV_DEV_BAD_DRAFT_LEN, SV_DEV_TIMEOUT, SV_DEV_BAD_PARENT) = (1 << b for b in range(9))
 SV_FLAG_Q_ZERO, SV_FLAG_Z_ZERO, SV_FLAG_INVALID = 1, 2, 4
@@ -57,6 +58,12 @@ _SIGS = {
                                            _vp]),
     "sv_verify_tree": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _u64, _u32, _vp, _c.c_int,
                                   _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sv_vocab_chunks": (_c.c_int, [_c.c_int, _c.c_int, _c.POINTER(_c.c_int), _c.POINTER(_c.c_int)]),
+    "sv_verify_regions": (_c.c_int, [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(_sz), _c.POINTER(_sz),
+                                     _c.POINTER(_sz), _c.POINTER(_sz), _c.POINTER(_sz)]),
+    "sv_verify_sample_phase": (_c.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _u64, _u32, _vp, _c.c_int, _c.c_int,
+                                          _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _vp, _vp, _vp, _vp,
+                                          _vp, _vp, _sz, _vp]),
     "sv_test_stall_next_verify": (None, [_c.c_int]),
     "sv_query_status": (_c.c_int, [_vp, _vp, _c.POINTER(_u32)]),
     "sv_status_string": (_c.c_char_p, [_c.c_int]),
@@ -313,6 +320,40 @@ def sv_verify_tree(target, t_row_stride, draft, d_row_stride, node_offsets, n_ro
                                 _p(parent), _p(tokens), _p(temperature), seed & (2 ** 64 - 1), round_,
                                 _p(request_ids), dt, B, Nmax, V, _p(out_path), _p(out_tokens), _p(out_accept_len),
                                 _p(out_flags), _p(ws), _ws_bytes(ws), _stream(stream)))
+
+
+def sv_vocab_chunks(V: int, dt: int) -> tuple[int, int]:
+    cl, nc = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().sv_vocab_chunks(V, dt, ctypes.byref(cl), ctypes.byref(nc)))
+    return cl.value, nc.value
+
+
+def sv_verify_regions(B: int, K: int, V: int, dt: int) -> dict:
+    """Workspace byte offsets and sizes of the chunk records and the two range-sum arrays."""
+    v = [ctypes.c_size_t(0) for _ in range(5)]
+    _check(lib().sv_verify_regions(B, K, V, dt, *(ctypes.byref(x) for x in v)))
+    return {"rec_offset": v[0].value, "rec_bytes": v[1].value, "mass_offset": v[2].value,
+            "mass_p_offset": v[3].value, "mass_bytes": v[4].value}
+
+
+def sv_verify_sample_phase(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round_,
+                           request_ids, dt, B, K, V, c_begin, c_end, phase, out_tokens, out_accept_len, out_p,
+                           out_q, out_flags, ws, stream=None) -> None:
+    if B > 0:
+        _need(target, "target", _logit_dtype(dt))
+        _need(draft, "draft", _logit_dtype(dt))
+        _need(draft_tokens, "draft_tokens", torch.int32, B * K)
+        _need(temperature, "temperature", torch.float32, B)
+        _need(request_ids, "request_ids", torch.int32, B)
+        _need(out_tokens, "out_tokens", torch.int32, B * (K + 1))
+        _need(out_accept_len, "out_accept_len", torch.int32, B)
+        _need(out_p, "out_p", torch.float32, B * K)
+        _need(out_q, "out_q", torch.float32, B * K)
+        _need(out_flags, "out_flags", torch.uint8, B)
+    _check(lib().sv_verify_sample_phase(_p(target), t_row_stride, _p(draft), d_row_stride, _p(draft_tokens),
+                                        _p(temperature), seed & (2 ** 64 - 1), round_, _p(request_ids), dt, B, K, V,
+                                        c_begin, c_end, phase, _p(out_tokens), _p(out_accept_len), _p(out_p),
+                                        _p(out_q), _p(out_flags), _p(ws), _ws_bytes(ws), _stream(stream)))
 
 
 def sv_test_stall_next_verify(wait_limit_ms: int) -> None:

@@ -2,6 +2,7 @@
 // Every check here runs on the host before any CUDA call, so an invalid call touches no GPU.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -73,7 +74,7 @@ std::atomic<int> g_stall_ms{0};
 
 // ---- shared verify entry ----------------------------------------------------------------------
 sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws, size_t ws_bytes,
-                        void* stream) {
+                        void* stream, int phase = -1) {
   if (p.B == 0) return SV_OK;  // nothing to verify: no workspace needed, nothing enqueued
   int cl, nc;
   sv::vocab_tiling(p.V, dt, &cl, &nc);
@@ -83,6 +84,15 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
   unsigned char* w = static_cast<unsigned char*>(ws);
   p.chunk_len = cl;
   p.nchunks = nc;
+  if (phase < 0) {  // a whole call: every chunk of every row
+    p.c_begin = 0;
+    p.c_end = nc;
+    p.v_begin = 0;
+  } else {
+    if (p.c_begin < 0 || p.c_end > nc || p.c_begin >= p.c_end)
+      return fail(SV_ERR_INVALID_ARG, "chunk range [%d, %d) outside [0, %d)", p.c_begin, p.c_end, nc);
+    p.v_begin = static_cast<int64_t>(p.c_begin) * cl;
+  }
   p.rows_per_req = 2 * p.Kmax + 1;
   // Greedy fixed-K calls need no per-request plan: every request has the same rows.  Sampling
   // calls take the per-request plan, which leaves out the draft rows of T == 0 requests.
@@ -96,7 +106,8 @@ sv_status verify_common(sv::VerifyParams& p, sv_dtype dt, bool sampled, void* ws
   p.rec = reinterpret_cast<sv::ChunkRecord*>(w + L.rec);
   p.mass = reinterpret_cast<float*>(w + L.mass);
   p.mass_p = reinterpret_cast<float*>(w + L.mass_p);
-  const int e = p.tree ? sv::launch_tree(p, dt, stream) : sv::launch_verify(p, dt, sampled, stream);
+  const int e = phase >= 0 ? sv::launch_phase(p, dt, phase, stream)
+                 : p.tree ? sv::launch_tree(p, dt, stream) : sv::launch_verify(p, dt, sampled, stream);
   if (e != 0) return cuda_fail(e, "verify launch");
   return SV_OK;
 }
@@ -217,14 +228,11 @@ sv_status sv_verify_greedy(const void* target, int64_t t_row_stride, const void*
   return verify_common(p, dt, false, ws, ws_bytes, stream);
 }
 
-sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
-                           const int32_t* draft_tokens, const float* temperature, uint64_t seed, uint32_t round,
-                           const int32_t* request_ids, sv_dtype dt, int B, int K, int V, int32_t* out_tokens,
-                           int32_t* out_accept_len, float* out_p, float* out_q, uint8_t* out_flags, void* ws,
-                           size_t ws_bytes, void* stream) {
-  sv_status s = sv::validate_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, dt, B, K,
-                                    V, out_tokens, out_accept_len);
-  if (s != SV_OK) return s;
+static sv::VerifyParams sample_params(const void* target, int64_t t_row_stride, const void* draft,
+                                      int64_t d_row_stride, const int32_t* draft_tokens, const float* temperature,
+                                      uint64_t seed, uint32_t round, const int32_t* request_ids, int B, int K, int V,
+                                      int32_t* out_tokens, int32_t* out_accept_len, float* out_p, float* out_q,
+                                      uint8_t* out_flags) {
   sv::VerifyParams p = {};
   p.target = target;
   p.t_row_stride = t_row_stride;
@@ -245,7 +253,68 @@ sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void*
   p.out_q = out_q;
   p.out_flags = out_flags;
   p.t_rows = p.d_rows = -1;
+  return p;
+}
+
+sv_status sv_verify_sample(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                           const int32_t* draft_tokens, const float* temperature, uint64_t seed, uint32_t round,
+                           const int32_t* request_ids, sv_dtype dt, int B, int K, int V, int32_t* out_tokens,
+                           int32_t* out_accept_len, float* out_p, float* out_q, uint8_t* out_flags, void* ws,
+                           size_t ws_bytes, void* stream) {
+  sv_status s = sv::validate_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, dt, B, K,
+                                    V, out_tokens, out_accept_len);
+  if (s != SV_OK) return s;
+  sv::VerifyParams p = sample_params(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round,
+                                     request_ids, B, K, V, out_tokens, out_accept_len, out_p, out_q, out_flags);
   return verify_common(p, dt, true, ws, ws_bytes, stream);
+}
+
+sv_status sv_vocab_chunks(int V, sv_dtype dt, int* chunk_len, int* nchunks) {
+  if (V < 1 || V > (1 << 30) || (dt != SV_BF16 && dt != SV_F32) || chunk_len == nullptr || nchunks == nullptr)
+    return fail(SV_ERR_INVALID_ARG, "sv_vocab_chunks: V=%d dt=%d", V, (int)dt);
+  sv::vocab_tiling(V, dt, chunk_len, nchunks);
+  return SV_OK;
+}
+
+sv_status sv_verify_regions(int B, int K, int V, sv_dtype dt, size_t* rec_offset, size_t* rec_bytes,
+                            size_t* mass_offset, size_t* mass_p_offset, size_t* mass_bytes) {
+  if (B < 1 || B > SV_MAX_BATCH || K < 0 || K > SV_MAX_DRAFT || V < 1 || V > (1 << 30) ||
+      (dt != SV_BF16 && dt != SV_F32))
+    return fail(SV_ERR_INVALID_ARG, "sv_verify_regions: B=%d K=%d V=%d dt=%d", B, K, V, (int)dt);
+  int cl, nc;
+  sv::vocab_tiling(V, dt, &cl, &nc);
+  const sv::VerifyLayout L = sv::verify_layout(B, K, nc);
+  if (rec_offset) *rec_offset = L.rec;
+  if (rec_bytes) *rec_bytes = sizeof(sv::ChunkRecord) * static_cast<size_t>(B) * (2 * static_cast<size_t>(K) + 1) * nc;
+  if (mass_offset) *mass_offset = L.mass;
+  if (mass_p_offset) *mass_p_offset = L.mass_p;
+  if (mass_bytes) *mass_bytes = sizeof(float) * static_cast<size_t>(B) * nc * sv::kDrawRanges;
+  return SV_OK;
+}
+
+sv_status sv_verify_sample_phase(const void* target, int64_t t_row_stride, const void* draft, int64_t d_row_stride,
+                                 const int32_t* draft_tokens, const float* temperature, uint64_t seed,
+                                 uint32_t round, const int32_t* request_ids, sv_dtype dt, int B, int K, int V,
+                                 int c_begin, int c_end, int phase, int32_t* out_tokens, int32_t* out_accept_len,
+                                 float* out_p, float* out_q, uint8_t* out_flags, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (phase < SV_PHASE_STATS || phase > SV_PHASE_PICK) return fail(SV_ERR_INVALID_ARG, "unknown phase %d", phase);
+  if (V < 1 || V > (1 << 30) || (dt != SV_BF16 && dt != SV_F32)) return fail(SV_ERR_INVALID_ARG, "V=%d dt=%d", V, (int)dt);
+  int cl, nc;
+  sv::vocab_tiling(V, dt, &cl, &nc);
+  if (c_begin < 0 || c_end > nc || c_begin >= c_end)
+    return fail(SV_ERR_INVALID_ARG, "chunk range [%d, %d) outside [0, %d)", c_begin, c_end, nc);
+  // the arrays hold this range's columns: rows need at least that many entries
+  const int V_local = static_cast<int>(std::min<int64_t>(V, static_cast<int64_t>(c_end) * cl) -
+                                       static_cast<int64_t>(c_begin) * cl);
+  sv_status s = sv::validate_sample(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, dt, B, K,
+                                    V_local, out_tokens, out_accept_len);
+  if (s != SV_OK) return s;
+  sv::VerifyParams p = sample_params(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round,
+                                     request_ids, B, K, V, out_tokens, out_accept_len, out_p, out_q, out_flags);
+  p.c_begin = c_begin;
+  p.c_end = c_end;
+  return verify_common(p, dt, true, ws, ws_bytes, stream, phase);
 }
 
 sv_status sv_verify_ragged(const void* target, int64_t t_row_stride, const int32_t* t_row_offsets, int64_t t_rows,

@@ -89,6 +89,10 @@ struct VerifyParams {
   const int32_t* tree_parent;  // [sum N_i] parent node per node
   const int32_t* tree_tokens;  // [sum N_i] drafted token per node
   int32_t* out_path;           // [B, Kmax + 1] accepted nodes
+  // vocabulary shard (a range of chunks; the whole row by default): the stream and the draw read
+  // chunks [c_begin, c_end), whose columns start at v_begin in the logit arrays given
+  int32_t c_begin, c_end;
+  int64_t v_begin;
   uint64_t wait_limit_ns;   // bound of every wait in the stream kernel
   int32_t stall_cta;        // test hook: > 0 makes CTA stall_cta - 1 of the stream issue no copy
   int32_t uniform_rows;     // > 0: every request has this many record rows (no per-request plan)
@@ -133,6 +137,8 @@ void vocab_tiling(int V, sv_dtype dt, int* chunk_len, int* nchunks);
 
 // Launchers (return cudaError_t as int to keep CUDA headers out of this file).
 int launch_verify(const VerifyParams& p, sv_dtype dt, bool sampled, void* stream);
+// One step of a sampled verification over a vocabulary shard (SV_PHASE_*).
+int launch_phase(const VerifyParams& p, sv_dtype dt, int phase, void* stream);
 // The streaming kernel alone (its records feed the tree walk).
 int launch_stats(const VerifyParams& p, sv_dtype dt, void* stream);
 // Tree verification: the streaming kernel, then the walk kernel behind it.

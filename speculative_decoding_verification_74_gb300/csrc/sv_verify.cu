@@ -175,10 +175,18 @@ __device__ __forceinline__ void locate_row(const int* row_start, const uint16_t*
   rr.rec_row = rr.is_target ? rr.k : Kmax + 1 + rr.k;
 }
 
+// Address of vocabulary entry 0 of a row when the arrays hold the columns from v_begin on (a
+// vocabulary shard; v_begin = 0 for whole rows): only entries >= v_begin are ever read through it.
+template <int DT>
+__device__ __forceinline__ const char* shard_row(const char* row, const VerifyParams& p) {
+  constexpr int kElt = DT == SV_BF16 ? 2 : 4;
+  return row - p.v_begin * kElt;
+}
+
 template <int DT>
 __device__ __forceinline__ const char* row_base(const VerifyParams& p, const RowRef& rr) {
-  return rr.is_target ? row_ptr<DT>(p.target, target_row(p, rr.i, rr.k), p.t_row_stride)
-                      : row_ptr<DT>(p.draft, draft_row(p, rr.i, rr.k), p.d_row_stride);
+  return shard_row<DT>(rr.is_target ? row_ptr<DT>(p.target, target_row(p, rr.i, rr.k), p.t_row_stride)
+                                    : row_ptr<DT>(p.draft, draft_row(p, rr.i, rr.k), p.d_row_stride), p);
 }
 
 // Closed-form plan: every request has U record rows (its K + 1 target rows, then its K draft
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
   constexpr uint32_t kPadWord = DT == SV_BF16 ? 0xFF80FF80u : 0xFF800000u;
   extern __shared__ __align__(128) unsigned char smem[];
   const int B = p.B, Kmax = p.Kmax, NC = p.nchunks, R = p.rows_per_req;
+  const int c_lo = p.c_begin, c_hi = p.c_end, NCo = c_hi - c_lo;  // this call's chunks of every row
   unsigned char* stages = smem;
   int* row_start = reinterpret_cast<int*>(smem + kStages * kStageBytes);        // [B + 1]
   uint16_t* info = reinterpret_cast<uint16_t*>(row_start + ((B + 4) & ~3));     // [B]
@@ -269,7 +278,7 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
   }
   __syncthreads();
   const int64_t rows_total = uniform ? static_cast<int64_t>(B) * p.uniform_rows : row_start[B];
-  const int64_t T = rows_total * NC;
+  const int64_t T = rows_total * NCo;
   const int64_t t0 = T * blockIdx.x / gridDim.x, t1 = T * (blockIdx.x + 1) / gridDim.x;
   if (t0 >= t1) {
     pdl_trigger();
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
   if (tid >= kConsumerThreads) {
     // ---------------- producer warp: one lane issues the bulk copies ----------------
     if (tid == kConsumerThreads) {
-      int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC);
+      int row = static_cast<int>(t0 / NCo), c = c_lo + static_cast<int>(t0 - static_cast<int64_t>(row) * NCo);
       int i = uniform ? 0 : find_request(row_start, B, row);
       RowRef rr;
       locate(row, i, rr);
@@ -315,8 +324,8 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
                         static_cast<uint32_t>(sp.nvec) * 16u, &full_bar[stage],
                         (p.tree && rr.k == 0) ? pol_last : pol_first);
         }
-        if (++c == NC && t + 1 < t1) {
-          c = 0;
+        if (++c == c_hi && t + 1 < t1) {
+          c = c_lo;
           locate(++row, i, rr);
           src = row_base<DT>(p, rr);
         }
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
   }
 
   // ---------------- consumer warps ----------------
-  int row = static_cast<int>(t0 / NC), c = static_cast<int>(t0 - static_cast<int64_t>(row) * NC);
+  int row = static_cast<int>(t0 / NCo), c = c_lo + static_cast<int>(t0 - static_cast<int64_t>(row) * NCo);
   int i = uniform ? 0 : find_request(row_start, B, row);
   RowRef rr;
   locate(row, i, rr);
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
       }
     }
 
-    const bool row_end = (c == NC - 1) || (t + 1 == t1);
+    const bool row_end = (c == c_hi - 1) || (t + 1 == t1);
     if (row_end) {
       // reduce the piece across threads and write its record
 #pragma unroll
@@ -569,8 +578,8 @@ __global__ void __launch_bounds__(kStatsThreads, StreamShape<DT>::kCtasPerSm) ro
       row_open = false;
       if (stop) break;
     }
-    if (++c == NC && t + 1 < t1) {
-      c = 0;
+    if (++c == c_hi && t + 1 < t1) {
+      c = c_lo;
       locate(++row, i, rr);
     }
   }
@@ -1058,13 +1067,13 @@ __global__ void __launch_bounds__(kMassThreads) mass_kernel(const VerifyParams p
   __shared__ ReqState st;
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.y, c = blockIdx.x, NC = p.nchunks;
+  const int i = blockIdx.y, c = p.c_begin + blockIdx.x, NC = p.nchunks;  // this call's chunks
   if (tid == 0) st = p.req[i];
   __syncthreads();
   if (st.mode == kModeNone) return;
   const bool residual = st.mode == kModeResidual;
-  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
-  const char* drow = residual ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
+  const char* trow = shard_row<DT>(row_ptr<DT>(p.target, st.row_t, p.t_row_stride), p);
+  const char* drow = residual ? shard_row<DT>(row_ptr<DT>(p.draft, st.row_d, p.d_row_stride), p) : trow;
   const int c0 = c * p.chunk_len, len = min(p.chunk_len, p.V - c0);
   int lo, hi;
   warp_range(len, kMassWarps, warp, &lo, &hi);
@@ -1101,8 +1110,8 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
   const ReqState& st = sm.st;
   if (st.mode == kModeNone) return;
   const bool residual_mode = st.mode == kModeResidual;
-  const char* trow = row_ptr<DT>(p.target, st.row_t, p.t_row_stride);
-  const char* drow = residual_mode ? row_ptr<DT>(p.draft, st.row_d, p.d_row_stride) : trow;
+  const char* trow = shard_row<DT>(row_ptr<DT>(p.target, st.row_t, p.t_row_stride), p);
+  const char* drow = residual_mode ? shard_row<DT>(row_ptr<DT>(p.draft, st.row_d, p.d_row_stride), p) : trow;
 
   // the crossing range (one warp)
   if (warp == 0) {
@@ -1139,8 +1148,10 @@ __global__ void __launch_bounds__(kPickThreads) pick_kernel(const VerifyParams p
   }
   __syncthreads();
 
-  // the entry inside the crossing range (whole CTA)
+  // the entry inside the crossing range (whole CTA), by the call that holds its chunk (a vocabulary
+  // shard that does not leaves the token to the one that does)
   const int estar = sm.chunk, cstar = estar / kDrawRanges;
+  if (cstar < p.c_begin || cstar >= p.c_end) return;
   const bool residual = !sm.bonus;
   const int c0 = cstar * p.chunk_len;
   int lo, hi;
@@ -1225,8 +1236,9 @@ cudaError_t launch_row_stats_t(const VerifyParams& p, cudaStream_t stream) {
     return e;
   // one contiguous task range per CTA; with a known task count (fixed-K calls) every CTA gets the
   // same number of (row, chunk) tasks, so the grid's CTAs finish together
-  const int64_t slots = static_cast<int64_t>(p.B) * p.rows_per_req * p.nchunks;
-  const int64_t tasks = p.uniform_rows > 0 ? static_cast<int64_t>(p.B) * p.uniform_rows * p.nchunks : slots;
+  const int nco = p.c_end - p.c_begin;  // chunks of every row this call streams
+  const int64_t slots = static_cast<int64_t>(p.B) * p.rows_per_req * nco;
+  const int64_t tasks = p.uniform_rows > 0 ? static_cast<int64_t>(p.B) * p.uniform_rows * nco : slots;
   const int64_t cap = static_cast<int64_t>(num_sms) * (nb > 0 ? nb : 1);
   const int64_t per_cta = (tasks + cap - 1) / cap;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, (tasks + per_cta - 1) / per_cta)));
@@ -1247,10 +1259,29 @@ cudaError_t launch_verify_t(const VerifyParams& p, bool sampled, cudaStream_t st
     return e;
   if (!sampled) return cudaSuccess;
   if (!p.fuse_draw &&
-      (e = launch_pdl(mass_kernel<DT>, dim3(p.nchunks, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p)) !=
+      (e = launch_pdl(mass_kernel<DT>, dim3(p.c_end - p.c_begin, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p)) !=
           cudaSuccess)
     return e;
   return launch_pdl(pick_kernel<DT>, dim3(p.B), kPickThreads, 0, stream, SV_KERNEL_PICK, p);
+}
+
+// One step of a sampled verification over a vocabulary shard (row f4): the stream of this
+// shard's chunks, the accept chain over every chunk's records, this shard's draw weights, or the
+// draw.
+template <int DT>
+cudaError_t launch_phase_t(const VerifyParams& p, int phase, cudaStream_t stream) {
+  switch (phase) {
+    case SV_PHASE_STATS:
+      return launch_row_stats_t<DT>(p, stream);
+    case SV_PHASE_ACCEPT: {
+      const size_t csmem = fin_layout(p.rows_per_req, p.nchunks, p.Kmax).bytes;
+      return launch_pdl(combine_kernel<DT>, dim3(1, p.B), kCombineThreads, csmem, stream, SV_KERNEL_COMBINE, p);
+    }
+    case SV_PHASE_WEIGHTS:
+      return launch_pdl(mass_kernel<DT>, dim3(p.c_end - p.c_begin, p.B), kMassThreads, 0, stream, SV_KERNEL_MASS, p);
+    default:
+      return launch_pdl(pick_kernel<DT>, dim3(p.B), kPickThreads, 0, stream, SV_KERNEL_PICK, p);
+  }
 }
 
 }  // namespace
@@ -1294,6 +1325,13 @@ VerifyLayout verify_layout(int B, int Kmax, int nchunks) {
 int launch_stats(const VerifyParams& p, sv_dtype dt, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return static_cast<int>(dt == SV_BF16 ? launch_row_stats_t<SV_BF16>(p, s) : launch_row_stats_t<SV_F32>(p, s));
+}
+
+int launch_phase(const VerifyParams& p_in, sv_dtype dt, int phase, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VerifyParams p = p_in;
+  p.fuse_draw = 0;  // the draw weights come from the shards' own weights step
+  return static_cast<int>(dt == SV_BF16 ? launch_phase_t<SV_BF16>(p, phase, s) : launch_phase_t<SV_F32>(p, phase, s));
 }
 
 int launch_verify(const VerifyParams& p_in, sv_dtype dt, bool sampled, void* stream) {
