@@ -5,7 +5,9 @@
 // The streaming kernel first reduces every node row of the call (target rows of all nodes, draft
 // rows of the sampled requests' nodes) into chunk records, as it does for a chain.  The walk
 // kernel then walks each request from the root (on a cluster of CTAs, below):
-//   * a node's row statistics come from its chunk records (max, sum of 2^(x k - c), argmax);
+//   * every node row's statistics (max, sum of 2^(x k - c), argmax) are merged from its chunk
+//     records up front, one row per warp across the cluster, and shared through distributed
+//     shared memory;
 //   * the accept test of a child needs p and q at the child's token only: two logits;
 //   * after j rejections at a node, the renormalised residual p' = norm(max(0, p' - q)) is
 //     max(0, p - a_j q) / N_j with a_0 = 0, N_0 = 1, a_{j+1} = a_j + N_j and
@@ -16,8 +18,9 @@
 // A request's walk runs on a cluster of 7 CTAs: every CTA takes the same decisions (same records,
 // same logits, same Philox uniforms), and each pass is split across them by vocabulary chunk, each
 // CTA streaming its chunks of the two rows through a 2-stage ring of 1-D bulk copies
-// (cp.async.bulk); the range sums meet in the workspace behind cluster barriers, and every CTA
-// adds them up in the same order.
+// (cp.async.bulk) and summing them with 16-byte shared-memory loads and packed f32x2 arithmetic;
+// the range sums meet in the workspace behind cluster barriers, and every CTA adds them up in the
+// same order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -161,15 +164,82 @@ __device__ __forceinline__ float weight(float tx, float dx, const Weights& w) {
   return fmaxf(0.0f, __fmaf_rn(pv, w.inv_st, -ex2_approx(__fmaf_rn(dx, w.kscale, -w.cd)) * w.qs));
 }
 
+// Packed float pairs beyond the streaming kernel's set: a product, and the distributed shared
+// memory of a cluster (the address of a variable in another CTA of the cluster, and a 16-byte load
+// from there).
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The weights of staged vectors [v_lo, v_hi) of a chunk (16 bytes each, target in ts, draft in
+// ds), lanes striding by 32, summed per lane: the same weight() per element, computed two at a
+// time in packed f32x2 registers (fma, mul and add round each half like the scalar operation).
+template <int DT>
+__device__ __forceinline__ float weight_sum_vec(const unsigned char* ts, const unsigned char* ds, int v_lo, int v_hi,
+                                                int lane, const Weights& w) {
+  const f32x2 k2 = f2_pack(w.kscale, w.kscale), nct2 = f2_pack(-w.ct, -w.ct), ncd2 = f2_pack(-w.cd, -w.cd);
+  const f32x2 ist2 = f2_pack(w.inv_st, w.inv_st), nqs2 = f2_pack(-w.qs, -w.qs);
+  f32x2 acc[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
+  auto add_pair = [&](int slot, f32x2 t2, f32x2 d2) {
+    const f32x2 pt = f2_exp2_offset(t2, k2, nct2);
+    if (!w.residual) {
+      acc[slot] = f2_add(acc[slot], pt);
+      return;
+    }
+    float r0, r1;
+    f2_unpack(f2_fma(pt, ist2, f2_mul(f2_exp2_offset(d2, k2, ncd2), nqs2)), r0, r1);
+    acc[slot] = f2_add(acc[slot], f2_pack(fmaxf(0.0f, r0), fmaxf(0.0f, r1)));
+  };
+  for (int v = v_lo + lane; v < v_hi; v += 32) {
+    const uint4 tv = lds128(ts + static_cast<size_t>(v) * 16);
+    const uint4 dv = w.residual ? lds128(ds + static_cast<size_t>(v) * 16) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t tw[4] = {tv.x, tv.y, tv.z, tv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    if constexpr (DT == SV_BF16) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        add_pair(e & 1, f2_pack(bf16_lo(tw[e]), bf16_hi(tw[e])), f2_pack(bf16_lo(dw[e]), bf16_hi(dw[e])));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        add_pair(e, f2_pack(__uint_as_float(tw[2 * e]), __uint_as_float(tw[2 * e + 1])),
+                 f2_pack(__uint_as_float(dw[2 * e]), __uint_as_float(dw[2 * e + 1])));
+    }
+  }
+  float a0, a1, a2, a3;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], a2, a3);
+  return (a0 + a1) + (a2 + a3);
+}
+
 struct WalkSmem {
-  float mt, st, md, sd;  // row statistics of the current node
-  int gt;
   int accept;            // the current child's test
   float Z;               // the last pass's total weight
   int y;                 // the drawn / emitted token
   int nkids;             // children of the current node
   int estar;             // pick: the crossing range
   float before;          // pick: the weight before it
+  float ssub[kWalkWarps];  // pick: the crossing range's weight in sub-ranges, one per warp
+  int slast[kWalkWarps];   // pick: the last entry with weight > 0 in each sub-range (-1: none)
   uint32_t flags, bad;
   int stop;              // the walk is over (or was aborted)
   int aborted;
@@ -189,12 +259,16 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   int* kid = path + Nmax;   // [Nmax] children of the current node, in order
   float* kp = reinterpret_cast<float*>(kid + Nmax);  // [Nmax] p at each child's token
   float* kq = kp + Nmax;                             // [Nmax] q at each child's token
+  // [2 Nmax] row statistics (max, sum, argmax) of every node row: target row of node n at n,
+  // draft row at Nmax + n
+  float4* rst = reinterpret_cast<float4*>(kq + Nmax);
   __shared__ __align__(8) uint64_t full_bar[kWalkStages];
   __shared__ WalkSmem ws;
   pdl_wait();  // the streaming kernel's records are complete
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x / kCluster, crank = blockIdx.x % kCluster;  // request, rank in its cluster
+  const int i = blockIdx.x / kCluster;                       // request
+  const int crank = static_cast<int>(cluster_rank());        // rank in its cluster
   const int NC = p.nchunks, R = 2 * p.Kmax + 1;
   int32_t* out_path = p.out_path + static_cast<int64_t>(i) * Nmax;
   int32_t* out_tok = p.out_tokens + static_cast<int64_t>(i) * Nmax;
@@ -254,6 +328,19 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   const float kscale = sampled ? kscale_of(T) : 0.0f;
   const int rid = p.request_ids ? __ldg(p.request_ids + i) : i;
   const ChunkRecord* recs = p.rec + static_cast<int64_t>(i) * R * NC;
+  // Row statistics of every node row, merged from the chunk records up front, one row per warp
+  // across the cluster (row j: target row of node j for j < N, else draft row of node j - N; a
+  // sampled tree's draft rows are those of nodes 0..N-2), so no node visit waits on records.
+  // Row j belongs to CTA (j / warps) mod kCluster; the others fetch it after the barrier below.
+  const int nrows = sampled ? 2 * N - 1 : N;
+  for (int j = crank * kWalkWarps + warp; j < nrows; j += kCluster * kWalkWarps) {
+    const bool drow = j >= N;
+    const int node = drow ? j - N : j;
+    float m, sum;
+    int g;
+    merge_row(recs + static_cast<int64_t>(drow ? p.Kmax + 1 + node : node) * NC, NC, sampled, kscale, &m, &sum, &g);
+    if (lane == 0) rst[(drow ? Nmax : 0) + node] = make_float4(m, sum, __int_as_float(g), 0.0f);
+  }
   // range sums, double-buffered across passes: a pass writes one buffer while no CTA can still be
   // reading it (every CTA read the other pass's sums before the barrier that ended that pass)
   float* const mass0 = p.mass + static_cast<int64_t>(i) * NC * kDrawRanges;
@@ -265,7 +352,14 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(p.req + i);
   if (crank == 0 && tid == 0) *abort_word = 0;
   __syncthreads();
-  cluster_sync();  // the word is clear before any CTA may set it
+  cluster_sync();  // the word is clear before any CTA may set it; every CTA's rows are merged
+  for (int j = tid; j < nrows; j += kWalkThreads) {  // the other CTAs' rows, from their shared memory
+    const int owner = (j / kWalkWarps) % kCluster;
+    if (owner == crank) continue;
+    const int idx = j >= N ? Nmax + (j - N) : j;
+    rst[idx] = ld_cluster_f4(cluster_addr(rst + idx, static_cast<uint32_t>(owner)));
+  }
+  __syncthreads();
 
   uint32_t it = 0;  // ring stages consumed so far (every thread keeps the same count)
   // One pass over a node's rows with weights w: the range sums (mass) and their total (ws.Z).
@@ -305,10 +399,19 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
       int lo, hi;
       range_of(len, warp, &lo, &hi);
       float sum = 0.0f;
-      for (int e = lo + lane; e < hi; e += 32) {
-        const float tx = staged<DT>(sb, trow, c0, e, st);
-        const float dx = w.residual ? staged<DT>(sb + kStageBytes, drow, c0, e, sd) : 0.0f;
-        sum += weight(tx, dx, w);
+      // a chunk staged whole (both rows) with this warp's range on vector boundaries: 16-byte
+      // loads and packed arithmetic; otherwise element by element
+      constexpr int kVec = 16 / kElt;
+      const bool whole = st.head == 0 && st.nvec * kVec == len &&
+                         (!w.residual || (sd.head == 0 && sd.nvec * kVec == len)) && lo % kVec == 0 && hi % kVec == 0;
+      if (whole) {
+        sum = weight_sum_vec<DT>(sb, sb + kStageBytes, lo / kVec, hi / kVec, lane, w);
+      } else {
+        for (int e = lo + lane; e < hi; e += 32) {
+          const float tx = staged<DT>(sb, trow, c0, e, st);
+          const float dx = w.residual ? staged<DT>(sb + kStageBytes, drow, c0, e, sd) : 0.0f;
+          sum += weight(tx, dx, w);
+        }
       }
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o2);
@@ -390,25 +493,66 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
       for (int e = lo + tid; e < hi; e += kWalkThreads)
         swt[e - lo] = weight(load_logit<DT>(trow, c0 + e), w.residual ? load_logit<DT>(drow, c0 + e) : 0.0f, w);
     __syncthreads();
-    if (warp == 0 && crank == 0) {  // the entry inside the range
-      float run2 = ws.before;
-      int y = -1, ylast = -1;
-      for (int e0 = lo; e0 < hi && y < 0; e0 += 32) {
-        const int e = e0 + lane;
-        const float wv = e < hi ? swt[e - lo] : 0.0f;
-        float incl = wv;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const float yv = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
-          if (lane >= o2) incl += yv;
-        }
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, e < hi && wv > 0.0f && run2 + incl > thr);
-        const unsigned pos = __ballot_sync(0xFFFFFFFFu, e < hi && wv > 0.0f);
-        if (hit) y = c0 + e0 + __ffs(hit) - 1;
-        else if (pos) ylast = c0 + e0 + 31 - __clz(pos);
-        run2 += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    // The range in one sub-range per warp: each warp sums its own; warp 0 then finds the sub-range
+    // where the running sum passes thr and scans only that one.
+    const int n = hi - lo, sub = (n + kWalkWarps - 1) / kWalkWarps;
+    if (crank == 0) {
+      const int s_lo = min(n, warp * sub), s_hi = min(n, s_lo + sub);
+      float acc = 0.0f;
+      int lastp = -1;
+      for (int e = s_lo + lane; e < s_hi; e += 32) {
+        const float wv = swt[e];
+        acc += wv;
+        if (wv > 0.0f) lastp = e;
       }
-      if (lane == 0) ws.y = y >= 0 ? y : (ylast >= 0 ? ylast : c0 + lo);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) {
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o2);
+        lastp = max(lastp, __shfl_xor_sync(0xFFFFFFFFu, lastp, o2));
+      }
+      if (lane == 0) {
+        ws.ssub[warp] = acc;
+        ws.slast[warp] = lastp;
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && crank == 0) {  // the entry inside the range
+      const float sv = lane < kWalkWarps ? ws.ssub[lane] : 0.0f;
+      float incl = sv;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const float yv = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+        if (lane >= o2) incl += yv;
+      }
+      const float excl_up = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+      const float excl = lane == 0 ? 0.0f : excl_up;
+      const unsigned cross = __ballot_sync(0xFFFFFFFFu, lane < kWalkWarps && sv > 0.0f && ws.before + incl > thr);
+      int y = -1;
+      if (cross) {
+        const int sidx = __ffs(cross) - 1;
+        float run2 = ws.before + __shfl_sync(0xFFFFFFFFu, excl, sidx);
+        const int s_lo = min(n, sidx * sub), s_hi = min(n, s_lo + sub);
+        for (int e0 = s_lo; e0 < s_hi && y < 0; e0 += 32) {
+          const int e = e0 + lane;
+          const float wv = e < s_hi ? swt[e] : 0.0f;
+          float run = wv;
+#pragma unroll
+          for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const float yv = __shfl_up_sync(0xFFFFFFFFu, run, o2);
+            if (lane >= o2) run += yv;
+          }
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, e < s_hi && wv > 0.0f && run2 + run > thr);
+          if (hit) y = c0 + lo + e0 + __ffs(hit) - 1;
+          run2 += __shfl_sync(0xFFFFFFFFu, run, 31);
+        }
+        if (y < 0) y = c0 + lo + ws.slast[sidx];  // rounding: the sum passed thr at the sub-range's end
+      } else {  // rounding: the range ends at or below thr; its last entry with weight > 0
+        int lp = lane < kWalkWarps ? ws.slast[lane] : -1;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o2));
+        y = c0 + lo + (lp >= 0 ? lp : 0);
+      }
+      if (lane == 0) ws.y = y;
     }
     __syncthreads();
   };
@@ -417,28 +561,10 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   int node = 0, L = 0;
   for (int step = 0; step < N; ++step) {
     const bool kids = first[node] >= 0;
-    // row statistics of the node (target row: warp 0; draft row: warp 1)
-    if (warp == 0) {
-      float m, s;
-      int g;
-      merge_row(recs + static_cast<int64_t>(node) * NC, NC, sampled, kscale, &m, &s, &g);
-      if (lane == 0) {
-        ws.mt = m;
-        ws.st = s;
-        ws.gt = g;
-      }
-    } else if (warp == 1 && sampled && kids) {
-      float m, s;
-      int g;
-      merge_row(recs + static_cast<int64_t>(p.Kmax + 1 + node) * NC, NC, true, kscale, &m, &s, &g);
-      if (lane == 0) {
-        ws.md = m;
-        ws.sd = s;
-      }
-    }
-    __syncthreads();
+    const float4 tstat = rst[node];                                            // target row
+    const float4 dstat = sampled && kids ? rst[Nmax + node] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);  // draft row
     if (!sampled) {  // greedy: the first child holding the target argmax
-      const int g = ws.gt;
+      const int g = __float_as_int(tstat.z);
       int acc = -1;
       for (int c = first[node]; c >= 0; c = next[c])
         if (tokn[c] == g) {
@@ -459,10 +585,10 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
     const char* drow = kids ? node_row<DT>(p.draft, static_cast<int64_t>(o) + node, p.d_row_stride) : trow;
     Weights w;
     w.kscale = kscale;
-    w.ct = exp_offset(ws.mt, kscale);
-    w.inv_st = __frcp_rn(ws.st);
-    w.cd = kids ? exp_offset(ws.md, kscale) : 0.0f;
-    const float inv_sd = kids ? __frcp_rn(ws.sd) : 0.0f;
+    w.ct = exp_offset(tstat.x, kscale);
+    w.inv_st = __frcp_rn(tstat.y);
+    w.cd = kids ? exp_offset(dstat.x, kscale) : 0.0f;
+    const float inv_sd = kids ? __frcp_rn(dstat.y) : 0.0f;
     const float u_draw = philox_uniform_f(p.seed, static_cast<uint32_t>(node), static_cast<uint32_t>(rid), 1u, p.round);
     if (!kids) {  // a leaf: y ~ p
       w.residual = false;
@@ -538,6 +664,7 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
     break;
   }
   __syncthreads();
+  cluster_sync();          // no CTA leaves while another may still read its row statistics
   if (crank != 0) return;  // one CTA of the cluster writes the outputs
   // ---- outputs ----
   for (int j = tid; j < Nmax; j += kWalkThreads) {
@@ -557,8 +684,8 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   }
 }
 
-size_t walk_smem_bytes(int Nmax) {  // the ring, then six int and two float arrays of Nmax
-  return static_cast<size_t>(kWalkStages) * 2 * kStageBytes + 8 * sizeof(int) * static_cast<size_t>(Nmax);
+size_t walk_smem_bytes(int Nmax) {  // the ring, six int and two float arrays of Nmax, 2 Nmax float4
+  return static_cast<size_t>(kWalkStages) * 2 * kStageBytes + (8 * sizeof(int) + 2 * sizeof(float4)) * static_cast<size_t>(Nmax);
 }
 
 std::mutex g_tree_mu;
