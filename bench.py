@@ -4,8 +4,9 @@
                   [--also c2,c4,c5]
 
 One step = one verification round (plus the D-cut schedule for c4) over one batch of synthetic
-logits already resident in HBM, through the library's C ABI.  Rotating input sets whose total
-exceeds the 129 MB L2 keep every step's logits cold in L2.  Rank 0 prints one JSON line: the
+logits already resident in HBM, through the library's C ABI.  Rotating input sets keep every
+step's logits cold in L2: their logits exceed the 129 MB L2 twice over, and so do the rows the
+other sets read again after their stream (the draw, a tree walk).  Rank 0 prints one JSON line: the
 headline workload (default c3, B=64 K=16 V=151936 fp32, the largest stream) with its roofline,
 end-to-end and CPU-baseline legs, and the other workloads (--also) measured the same way under
 "other_workloads".
@@ -374,11 +375,16 @@ def measure_workload(workload, steps, warm, rank, world, dev, dist, *, full: boo
     import torch
     import speculative_decoding_verification_74_gb300 as sv
 
-    # rotating input sets: enough distinct sets that the working set exceeds L2
+    # Rotating input sets.  The stream's copies are marked evict-first in L2, so the lines a step
+    # reads at a higher priority (the rows the draw reads again; a tree walk's rows) can outlive the
+    # stream of the next set.  So there are enough sets that the logits read exceed L2 twice over,
+    # and that the other sets' re-read rows (at most 2 rows per request, 4 for a tree) exceed it
+    # twice over too: no step finds its own rows in L2 from its set's previous turn.
     probe = make_sets(workload, 1, rank_seed(1000, rank))
     b0 = probe[0]["batch"]
     set_bytes = algorithmic_bytes(b0, b0.keep_len if workload != "c4" else np.full(b0.B, 16))
-    n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))))
+    reread = b0.B * (4 if workload == "t1" else 2) * b0.V * (2 if b0.dtype == "bf16" else 4)
+    n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))), 1 + int(np.ceil(2.0 * L2_BYTES / reread)))
     n_sets = min(n_sets, 200)
     sets = probe + make_sets(workload, n_sets - 1, rank_seed(1001, rank))
     gw = GpuWorkload(workload, sets, dev)
