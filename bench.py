@@ -368,6 +368,19 @@ def cost_table_leg(gw, reps: int = 200) -> dict:
             "schedule_us": us, "timing": f"CUDA events over {reps} graph replays of one D-cut call"}
 
 
+def rotation_sets(workload: str, b0) -> int:
+    """How many input sets the timed steps rotate through.  The stream's copies are marked
+    evict-first in L2, so the lines a step reads at a higher priority (the rows the draw reads
+    again; a tree walk's rows) can outlive the stream of the next set.  So there are enough sets
+    that the logits read exceed L2 twice over, and that the other sets' re-read rows (at most 2
+    rows per request, 4 for a tree) exceed it twice over too: no step finds its own rows in L2
+    from its set's previous turn."""
+    set_bytes = algorithmic_bytes(b0, b0.keep_len if workload != "c4" else np.full(b0.B, 16))
+    reread = b0.B * (4 if workload == "t1" else 2) * b0.V * (2 if b0.dtype == "bf16" else 4)
+    n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))), 1 + int(np.ceil(2.0 * L2_BYTES / reread)))
+    return min(n_sets, 200)
+
+
 def measure_workload(workload, steps, warm, rank, world, dev, dist, *, full: bool) -> dict:
     """One workload's measurement on this rank: K timed steps (CUDA graphs, rotating input sets
     larger than L2), per-kernel durations, and, with `full`, the end-to-end leg.  Returns the
@@ -375,17 +388,8 @@ def measure_workload(workload, steps, warm, rank, world, dev, dist, *, full: boo
     import torch
     import speculative_decoding_verification_74_gb300 as sv
 
-    # Rotating input sets.  The stream's copies are marked evict-first in L2, so the lines a step
-    # reads at a higher priority (the rows the draw reads again; a tree walk's rows) can outlive the
-    # stream of the next set.  So there are enough sets that the logits read exceed L2 twice over,
-    # and that the other sets' re-read rows (at most 2 rows per request, 4 for a tree) exceed it
-    # twice over too: no step finds its own rows in L2 from its set's previous turn.
     probe = make_sets(workload, 1, rank_seed(1000, rank))
-    b0 = probe[0]["batch"]
-    set_bytes = algorithmic_bytes(b0, b0.keep_len if workload != "c4" else np.full(b0.B, 16))
-    reread = b0.B * (4 if workload == "t1" else 2) * b0.V * (2 if b0.dtype == "bf16" else 4)
-    n_sets = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, set_bytes))), 1 + int(np.ceil(2.0 * L2_BYTES / reread)))
-    n_sets = min(n_sets, 200)
+    n_sets = rotation_sets(workload, probe[0]["batch"])
     sets = probe + make_sets(workload, n_sets - 1, rank_seed(1001, rank))
     gw = GpuWorkload(workload, sets, dev)
 

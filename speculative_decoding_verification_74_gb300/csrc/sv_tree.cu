@@ -241,7 +241,6 @@ struct WalkSmem {
   float ssub[kWalkWarps];  // pick: the crossing range's weight in sub-ranges, one per warp
   int slast[kWalkWarps];   // pick: the last entry with weight > 0 in each sub-range (-1: none)
   uint32_t flags, bad;
-  int stop;              // the walk is over (or was aborted)
   int aborted;
 };
 
@@ -286,7 +285,6 @@ __global__ void __launch_bounds__(kWalkThreads) tree_walk_kernel(const VerifyPar
   if (tid == 0) {
     ws.bad = 0;
     ws.flags = 0;
-    ws.stop = 0;
     ws.aborted = 0;
     for (int s = 0; s < kWalkStages; ++s) mbar_init(&full_bar[s], 1);
     fence_proxy_async_smem();

@@ -1,5 +1,5 @@
-"""Host logic of bench.py (CPU only): algorithmic byte counts, the source hash that gates recorded
-DRAM traffic, and the clock sampler's windows and throttle reasons."""
+"""Host logic of bench.py (CPU only): algorithmic byte counts, the input-set rotation, the source
+hash that gates recorded DRAM traffic, and the clock sampler's windows and throttle reasons."""
 import datetime
 import json
 import os
@@ -29,6 +29,28 @@ def test_algorithmic_bytes_of_the_workloads():
     # greedy requests with given tokens read target rows only; T > 0 adds the draft rows
     mix = _batch("bf16", 3, 4, 1000, [0.0, 1.0, 0.6])
     assert bench.algorithmic_bytes(mix, [2, 4, 0]) == ((3) + (5 + 4) + (1 + 0)) * 1000 * 2
+
+
+def test_rotation_flushes_re_read_rows_from_l2():
+    # the logits read, and the rows the other sets read again after their stream, both exceed
+    # L2 twice over, so no step meets its own rows in L2 from its set's previous turn
+    L2 = bench.L2_BYTES
+    cases = {  # workload: (batch, re-read rows per request)
+        "c2": (_batch("bf16", 16, 3, 151936, [1.0] * 16), 2),
+        "c3": (_batch("f32", 64, 16, 151936, [0.6] * 64), 2),
+        "t1": (_batch("bf16", 64, 15, 151936, [1.0] * 64), 4),
+    }
+    for w, (b, rows) in cases.items():
+        b.keep_len = np.full(b.B, b.tokens.shape[1], np.int32)
+        n = bench.rotation_sets(w, b)
+        elt = 2 if b.dtype == "bf16" else 4
+        assert n >= 2 and n * bench.algorithmic_bytes(b, b.keep_len) >= 2 * L2, w
+        assert (n - 1) * b.B * rows * b.V * elt >= 2 * L2, w
+        assert (n - 2) * b.B * rows * b.V * elt < 2 * L2, w  # and no more sets than that needs
+    # C4's sets are sized by all 16 drafted positions, whatever the schedule keeps
+    c4 = _batch("bf16", 64, 16, 151936, [1.0] * 64)
+    c4.keep_len = np.zeros(64, np.int32)
+    assert bench.rotation_sets("c4", c4) == 1 + int(np.ceil(2 * L2 / (64 * 2 * 151936 * 2)))
 
 
 def _copy_sources(tmp_path):
