@@ -3,7 +3,9 @@
 // row_stats  One streaming pass over every logit row a round needs.  A persistent grid walks
 //            (request, row, vocabulary chunk) tasks in request-major order, one contiguous range
 //            per CTA; one producer lane issues 1-D bulk copies (cp.async.bulk) of <= 16 KB chunks
-//            into a 4-stage shared-memory ring and four consumer warps reduce each chunk.  A
+//            into a shared-memory ring (4 stages at 3 CTAs per SM for fp32 rows, 3 stages at 4
+//            CTAs per SM for bf16) and four consumer warps, each waiting on a stage itself,
+//            reduce each chunk.  A
 //            piece of a row (its chunks inside one CTA's range) becomes one record {max m,
 //            sum of 2^(x k - rint(m k)) with k = log2(e)/T, first argmax, logit at the drafted
 //            token}.  The kernel only streams and writes records: no atomics, no fences, no
