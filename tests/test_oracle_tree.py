@@ -6,6 +6,8 @@
     a threshold in its uniform, found by bisection) and over every drafted tree, the first L
     emitted tokens, completed by target draws, follow the target's law to 1e-9.
   * Greedy: brute force over every drafted tree on integer logits with ties.
+  * The walk's closed form of the repeated residual (what the library's walk sums in each pass)
+    equals the oracle's rule applied j times, in exact rational arithmetic.
 """
 import itertools
 
@@ -218,3 +220,51 @@ def test_greedy_brute_force_over_drafted_trees():
             node = nxt
         assert res["tokens"] == want
         assert res["accept_len"] == len(want) - 1
+
+
+# ------------------------------------------------------ the repeated residual in closed form
+
+
+def _iterated_residual(p, q, j):
+    """The oracle's rule after j rejections at one node: p' <- norm(max(0, p' - q)), j times."""
+    r = list(p)
+    for _ in range(j):
+        w = [max(0, a - b) for a, b in zip(r, q)]
+        z = sum(w)
+        if z == 0:
+            return None
+        r = [x / z for x in w]
+    return r
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_repeated_residual_closed_form(seed):
+    """After j rejections p' = max(0, p - a_j q) / N_j with a_0 = 0, N_0 = 1, a_{j+1} = a_j + N_j
+    and N_{j+1} = sum_v max(0, p_v - a_{j+1} q_v): one pass over the node's rows per rejection.
+    Checked exactly (fractions) on random rational distributions, for every j up to the first
+    zero-mass residual."""
+    from fractions import Fraction as F
+    rng = np.random.default_rng(seed)
+    V = int(rng.integers(3, 9))
+    pw, qw = rng.integers(0, 20, V) + 1, rng.integers(0, 20, V)
+    qw[rng.integers(1, V)] += 1
+    if seed % 2 == 0:
+        qw[0] = 0  # an entry q misses keeps the residual's mass above zero at every j
+    p = [F(int(x), int(pw.sum())) for x in pw]
+    q = [F(int(x), int(qw.sum())) for x in qw]
+    a, N = F(0), F(1)
+    checked = 0
+    for j in range(8):
+        it = _iterated_residual(p, q, j)
+        if it is None:
+            break
+        closed = [max(F(0), pv - a * qv) / N for pv, qv in zip(p, q)]
+        assert closed == it, (seed, j)
+        checked += 1
+        a_next = a + N
+        N_next = sum(max(F(0), pv - a_next * qv) for pv, qv in zip(p, q))
+        if N_next == 0:
+            break
+        a, N = a_next, N_next
+    assert checked >= (8 if seed % 2 == 0 else 2)
+
