@@ -339,9 +339,12 @@ def sv_verify_regions(B: int, K: int, V: int, dt: int) -> dict:
 def sv_verify_sample_phase(target, t_row_stride, draft, d_row_stride, draft_tokens, temperature, seed, round_,
                            request_ids, dt, B, K, V, c_begin, c_end, phase, out_tokens, out_accept_len, out_p,
                            out_q, out_flags, ws, stream=None) -> None:
-    if B > 0:
-        _need(target, "target", _logit_dtype(dt))
-        _need(draft, "draft", _logit_dtype(dt))
+    if B > 0 and K >= 0:
+        # the arrays hold the shard's columns: those of chunks [c_begin, c_end)
+        cl, nc = sv_vocab_chunks(V, dt)
+        v_local = min(V, c_end * cl) - c_begin * cl if 0 <= c_begin < c_end <= nc else 0
+        _need_rows(target, "target", dt, B * (K + 1), t_row_stride, v_local)
+        _need_rows(draft, "draft", dt, B * K, d_row_stride, v_local)
         _need(draft_tokens, "draft_tokens", torch.int32, B * K)
         _need(temperature, "temperature", torch.float32, B)
         _need(request_ids, "request_ids", torch.int32, B)

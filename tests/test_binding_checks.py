@@ -116,3 +116,25 @@ def test_greedy_and_empty_batch():
     empty = torch.empty((0, 4), dtype=torch.int32)
     _raises(lambda: sv.sv_verify_greedy(None, 0, None, 0, None, sv.SV_BF16, 0, 3, 100, empty, empty, None),
             DEVICE_MSG)
+
+
+def test_vocab_shard_checks():
+    # a shard's arrays hold the columns of its chunks: a shard of the first two chunks of a bf16
+    # row of V = 20000 holds 2 * chunk_len columns, and its rows are checked at that width
+    B, K, V = 2, 3, 20000
+    cl, nc = sv.sv_vocab_chunks(V, sv.SV_BF16)
+    assert nc >= 3
+    w = 2 * cl
+
+    def phase(target_rows=B * (K + 1), width=w, stride=w, c_end=2):
+        a = _sample_args(B, K, 1)
+        sv.sv_verify_sample_phase(torch.zeros(target_rows, width, dtype=torch.bfloat16), stride,
+                                  torch.zeros(B * K, width, dtype=torch.bfloat16), stride, a["tokens"],
+                                  a["temperature"], 1, 0, None, sv.SV_BF16, B, K, V, 0, c_end, sv.SV_PHASE_STATS,
+                                  *a["out"], None)
+
+    _raises(lambda: phase(), DEVICE_MSG)                                        # every check passes
+    _raises(lambda: phase(target_rows=B * (K + 1) - 1), "target holds")
+    _raises(lambda: phase(width=w - 1), "target holds")                         # narrower than the shard
+    _raises(lambda: phase(stride=V, c_end=3), "target holds")                   # a third chunk's columns
+
