@@ -58,7 +58,7 @@ def _worker(rank, world, port, budget, out):
 @pytest.mark.parametrize("budget", [0, 20])
 def test_two_ranks_see_the_single_process_schedule(budget):
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), budget, out), nprocs=world, join=True)
         res = dict(out)

@@ -50,7 +50,7 @@ def _worker(rank, world, port, nc, out):
 
 @pytest.mark.parametrize("world,nc", [(2, 19), (3, 38), (2, 2)])
 def test_two_ranks_gather_every_column(world, nc):
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _port(), nc, out), nprocs=world, join=True)
     assert all(out[r] for r in range(world))

@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 
 def test_two_rank_job_totals_and_seeds():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
